@@ -1,0 +1,143 @@
+"""Seeded synthetic inputs for MLA decode over a paged latent KV cache.
+
+This module holds no arithmetic of the method: it only draws the inputs (query,
+paged cache, block table, sequence lengths) that both the CUDA path and the CPU
+oracle consume, so that the two can be compared on identical bits.
+
+Recipe (one torch generator per case, seeded by the case's seed; draws happen
+in this order):
+  1. ``cache_seqlens``: the case's fixed list, or ``randint(lo, hi + 1)`` per
+     sequence for variable-length cases.
+  2. ``block_table``: a random permutation of the physical pool.  When the
+     pool has a page for every table entry, the table is that permutation
+     reshaped to [b, max_blocks]; otherwise the pages each sequence needs are
+     taken from it in order and the unused entries hold random pool pages
+     (never read by either side).  Either way a sequence's pages are scattered
+     over the pool.
+  3. ``q``: fp32 N(0, 1), rounded to bf16 (round to nearest even).
+  4. ``kcache``: fp32 N(0, 1), rounded to bf16.  Rows past a sequence's end in
+     its last page, and pool pages no sequence uses, hold the same finite
+     random values (callers may overwrite them to test robustness).
+
+Shapes follow the DeepSeek-style latent cache of the usage page ("FlashMLA란
+무엇인가?", sections "FlashMLA의 주요 특성" and "FlashMLA 설치 및 사용"):
+d = 576 (512 latent + 64 RoPE), dv = 512, page 64, one KV head.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional, Sequence
+
+import torch
+
+PAGE = 64
+D_QK = 576
+D_V = 512
+
+
+@dataclasses.dataclass(frozen=True)
+class Case:
+    """One decode workload."""
+    name: str
+    batch: int
+    s_q: int
+    h_q: int
+    seqlens: Optional[Sequence[int]] = None     # fixed lengths, or
+    seqlen_range: Optional[tuple] = None         # (lo, hi) inclusive, drawn per sequence
+    causal: bool = False
+    h_kv: int = 1
+    d: int = D_QK
+    dv: int = D_V
+    page: int = PAGE
+    pool_pages: Optional[int] = None             # physical pages; default = pages needed
+    seed: int = 0
+
+    @property
+    def softmax_scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def num_q_rows(self) -> int:
+        return self.s_q * self.h_q // self.h_kv
+
+
+# The five workloads of the benchmark and parity suite.
+TINY = Case("tiny", batch=2, s_q=1, h_q=16, seqlens=(100, 37), pool_pages=4, seed=0)
+UNIFORM = Case("uniform", batch=64, s_q=1, h_q=128, seqlens=(4096,) * 64, pool_pages=4096, seed=1)
+VARIABLE = Case("variable", batch=128, s_q=1, h_q=128, seqlen_range=(256, 16384), seed=2)
+MTP = Case("mtp", batch=32, s_q=8, h_q=128, seqlens=(8192,) * 32, causal=True, seed=3)
+LONG = Case("long", batch=64, s_q=1, h_q=128, seqlens=(65536,) * 64, seed=4)
+CASES = {c.name: c for c in (TINY, UNIFORM, VARIABLE, MTP, LONG)}
+
+
+@dataclasses.dataclass
+class Inputs:
+    case: Case
+    q: torch.Tensor              # [b, s_q, h_q, d] bf16
+    kcache: torch.Tensor         # [num_blocks, page, h_kv, d] bf16
+    block_table: torch.Tensor    # [b, max_blocks] int32
+    cache_seqlens: torch.Tensor  # [b] int32
+
+
+def draw_seqlens(case: Case, gen: torch.Generator) -> torch.Tensor:
+    if case.seqlens is not None:
+        if len(case.seqlens) != case.batch:
+            raise ValueError("seqlens must have one entry per sequence")
+        return torch.tensor(list(case.seqlens), dtype=torch.int32)
+    lo, hi = case.seqlen_range
+    return torch.randint(lo, hi + 1, (case.batch,), generator=gen, dtype=torch.int64).to(torch.int32)
+
+
+def make_inputs(case: Case, device: str = "cpu", seqlens: Optional[Sequence[int]] = None) -> Inputs:
+    """Draw the inputs of ``case``.
+
+    The small tensors (lengths, table) are always drawn on the CPU generator.
+    ``q`` and ``kcache`` are drawn with a generator on ``device``: on the CPU
+    this is bit-reproducible everywhere; on a CUDA device it is torch's own
+    seeded Philox generator, used for the multi-GB workloads.
+    """
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(case.seed)
+    sl = torch.tensor(list(seqlens), dtype=torch.int32) if seqlens is not None else draw_seqlens(case, gen)
+    if sl.numel() != case.batch:
+        raise ValueError("seqlens must have one entry per sequence")
+    n_pages = [(int(s) + case.page - 1) // case.page for s in sl.tolist()]
+    max_blocks = max(1, max(n_pages) if n_pages else 1)
+    needed = sum(n_pages)
+    pool = case.pool_pages if case.pool_pages is not None else needed
+    pool = max(pool, needed, 1)
+    perm = torch.randperm(pool, generator=gen).to(torch.int32)
+    if pool >= case.batch * max_blocks:
+        # the whole table is one permutation of the pool: every entry distinct
+        bt = perm[:case.batch * max_blocks].reshape(case.batch, max_blocks).clone()
+    else:
+        bt = torch.randint(0, pool, (case.batch, max_blocks), generator=gen, dtype=torch.int64).to(torch.int32)
+        cur = 0
+        for b, n in enumerate(n_pages):
+            bt[b, :n] = perm[cur:cur + n]
+            cur += n
+    if device == "cpu":
+        dgen = gen
+    else:
+        dgen = torch.Generator(device=device)
+        dgen.manual_seed(case.seed + 1_000_003)
+    q = torch.randn((case.batch, case.s_q, case.h_q, case.d), generator=dgen, device=device,
+                    dtype=torch.float32).to(torch.bfloat16)
+    kcache = torch.empty((pool, case.page, case.h_kv, case.d), dtype=torch.bfloat16, device=device)
+    # draw the pool in slabs to bound the fp32 temporary
+    slab = max(1, (1 << 27) // (case.page * case.h_kv * case.d))
+    for s in range(0, pool, slab):
+        e = min(pool, s + slab)
+        kcache[s:e] = torch.randn((e - s, case.page, case.h_kv, case.d), generator=dgen, device=device,
+                                  dtype=torch.float32).to(torch.bfloat16)
+    return Inputs(case, q, kcache, bt.to(device), sl.to(device))
+
+
+def kv_pages_touched(cache_seqlens, page: int = PAGE) -> int:
+    return sum((int(s) + page - 1) // page for s in cache_seqlens)
+
+
+def bf16_bits(t: torch.Tensor):
+    """uint16 numpy view of a CPU bf16 tensor's bit patterns."""
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")
