@@ -1,0 +1,423 @@
+"""Benchmark: MLA decode over a paged latent KV cache on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step is one pass of the whole path over one batch: the tile scheduler
+(mla_get_metadata), the split-KV kernel and the combine (mla_decode_kvcache),
+on inputs already resident in HBM.  The default workload is the uniform decode
+batch (b=64, s_q=1, h_q=128, 4096 cached tokens per sequence, page 64).
+
+Reported figures (one JSON line from rank 0):
+  value         KV-cache GB/s: bytes of the KV pages touched plus q, O and LSE,
+                divided by the device time of a step (the metric's bytes)
+  us_per_call   device time of a step in microseconds
+  tflops        2 * h_q * (576 + 512) * visible keys, per second
+  roofline      the split-KV kernel alone (CUDA events around it on its stream)
+                against the measured HBM copy bandwidth
+  e2e           the same metric through the public API with host buffers:
+                pinned host -> device copies of every input, the two calls,
+                device -> host copies of O and LSE, all inside the timed region
+  cpu_baseline  the fp64 oracle on the host cores, on a bounded sample
+
+The KV pages of every workload except the tiny one exceed the 129 MB L2, so
+no flush is done between steps (config.l2 says so).  --impl reference times
+the fp64 CPU oracle instead (this tier's reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+METRIC = "MLA decode µs/call, KV-cache GB/s and TFLOPS vs GB300 roofline"
+
+
+# ------------------------------------------------------------------ workload figures
+def workload_figures(case, seqlens):
+    """Algorithmic bytes and FLOPs of one decode call."""
+    from mla_decode_attention_latent_gb300 import workloads as W
+    page_bytes = case.page * case.h_kv * case.d * 2
+    kv_bytes = W.kv_pages_touched(seqlens, case.page) * page_bytes
+    q_bytes = case.batch * case.s_q * case.h_q * case.d * 2
+    o_bytes = case.batch * case.s_q * case.h_q * case.dv * 2
+    lse_bytes = case.batch * case.s_q * case.h_q * 4
+    keys = 0
+    for t in seqlens:
+        for i in range(case.s_q):
+            keys += max(0, (t - case.s_q + i + 1) if case.causal else t)
+    flops = 2.0 * case.h_q * (case.d + case.dv) * keys
+    return {"bytes": kv_bytes + q_bytes + o_bytes + lse_bytes, "kv_bytes": kv_bytes, "flops": flops,
+            "valid_token_bytes": sum(seqlens) * case.h_kv * case.d * 2}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            hbm = d.get("hbm_gbs")
+            bf16 = d.get("bf16_tflops")
+            bf16s = d.get("bf16_tflops_sustained")
+            if hbm:
+                return {"hbm_gbs": float(hbm), "bf16_tflops": float(bf16 or FALLBACK_BF16_TFLOPS),
+                        "bf16_tflops_sustained": float(bf16s or bf16 or FALLBACK_BF16_TFLOPS),
+                        "source": "measured"}
+        except Exception:
+            pass
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+            "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def split_kernel_traffic(workload):
+    """DRAM bytes per split-KV launch from the committed ncu summary, if the kernel is unchanged since."""
+    path = os.path.join(ROOT, "profiles", f"split_kv_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    if not m or not h or h.group(1) != split_source_hash():
+        return None
+    return float(m.group(1))
+
+
+def split_source_hash():
+    csrc = os.path.join(ROOT, "mla_decode_attention_latent_gb300", "csrc")
+    hs = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.startswith("mla_split") or name.endswith((".cuh", ".h")):
+            hs.update(open(os.path.join(csrc, name), "rb").read())
+    return hs.hexdigest()
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.25)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup(n_gpus):
+    if n_gpus <= 1 and "RANK" not in os.environ:
+        return 0, 1, 0
+    import torch.distributed as dist
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(n_gpus)))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    torch.cuda.set_device(local)
+    dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle
+def time_oracle(case, x_cpu, budget_s=10.0, max_seqs=None):
+    """Time the fp64 oracle on whole sequences (all rows) until ~budget_s of work; scale to one call."""
+    import numpy as np
+
+    import oracle
+    from mla_decode_attention_latent_gb300 import workloads as W
+    R = case.s_q * case.h_q
+    sl = x_cpu.cache_seqlens.numpy()
+    q_bits = W.bf16_bits(x_cpu.q)
+    k_bits = W.bf16_bits(x_cpu.kcache)
+    bt = x_cpu.block_table.numpy()
+
+    def run(seqs):
+        rows = np.concatenate([np.arange(b * R, (b + 1) * R, dtype=np.int64) for b in seqs])
+        t0 = time.perf_counter()
+        oracle.mla_decode(q_bits, k_bits, bt, sl, case.dv, case.softmax_scale, case.causal, rows=rows)
+        return time.perf_counter() - t0
+
+    t1 = run([0])
+    n = max(1, min(case.batch if max_seqs is None else max_seqs, int(budget_s / max(t1, 1e-6))))
+    seqs = list(range(n))
+    t = run(seqs)
+    frac_keys = sum(int(sl[b]) for b in seqs) / max(1, sum(int(s) for s in sl))
+    return {"seconds": t, "seqs": n, "call_seconds": t / frac_keys, "cores": oracle.max_threads()}
+
+
+# ------------------------------------------------------------------ main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="uniform")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    from mla_decode_attention_latent_gb300 import workloads as W
+    case = W.CASES[args.workload]
+
+    if args.impl == "reference":
+        return reference_arm(args, case)
+
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import mla_decode_attention_latent_gb300 as mla
+    mla._lib.load()
+
+    x = W.make_inputs(case, device=str(dev))
+    sl_list = x.cache_seqlens.cpu().tolist()
+    fig = workload_figures(case, sl_list)
+    stream = torch.cuda.current_stream(dev)
+
+    md, ns = mla.mla_get_metadata(x.cache_seqlens, case.num_q_rows, case.h_kv)
+    num_parts = md.shape[0]
+    o = torch.empty((case.batch, case.s_q, case.h_q, case.dv), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((case.batch, case.s_q, case.h_q), dtype=torch.float32, device=dev)
+    ws = torch.empty((mla.mla_workspace_bytes(case.batch, case.s_q, case.h_q, case.h_kv, case.dv, num_parts),),
+                     dtype=torch.uint8, device=dev)
+
+    def step():
+        mla.mla_get_metadata(x.cache_seqlens, case.num_q_rows, case.h_kv, num_parts=num_parts)
+        mla.mla_decode_kvcache(x.q, x.kcache, x.block_table, x.cache_seqlens, case.dv, md, ns,
+                               softmax_scale=case.softmax_scale, causal=case.causal, out=o, lse=lse, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert mla.mla_device_status(clear=True) == 0, "device-side error during warm-up"
+
+    # per-step split-kernel events (recorded by the library around the split-KV launch)
+    ev_split = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in ev_split:
+        a.record(stream)
+        b.record(stream)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for k in range(args.steps):
+        mla.mla_set_timing_events(*ev_split[k])
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    mla.mla_set_timing_events(None, None)
+    clk = clocks.stop()
+    assert mla.mla_device_status(clear=True) == 0, "device-side error in the timed region"
+
+    ms_total = start.elapsed_time(end)
+    ms_total = max_over_ranks(ms_total, world)
+    ms_step = ms_total / args.steps
+    split_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_split)
+    total_bytes = fig["bytes"] * world
+    value = total_bytes / (ms_step * 1e-3) / 1e9
+    tflops = fig["flops"] * world / (ms_step * 1e-3) / 1e12
+    pk = peaks()
+    bound = "hbm"
+    achieved = fig["bytes"] / (split_ms * 1e-3) / 1e9
+    traffic = split_kernel_traffic(args.workload)
+
+    # end-to-end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_run(mla, case, x, fig, dev, stream, steps=max(3, min(args.steps, 10)), world=world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        x_cpu = W.make_inputs(case, device="cpu") if case.name == "tiny" else \
+            W.Inputs(case, x.q.cpu(), x.kcache.cpu(), x.block_table.cpu(), x.cache_seqlens.cpu())
+        t = time_oracle(case, x_cpu)
+        cpu = {"value": fig["bytes"] / t["call_seconds"] / 1e9, "unit": "GB/s", "cores": t["cores"],
+               "kind": "oracle", "us_per_call": t["call_seconds"] * 1e6,
+               "sample": f"{t['seqs']} of {case.batch} sequences (all {case.s_q * case.h_q} query rows each), "
+                         f"{t['seconds']:.2f} s, scaled to one call by visible keys"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "us_per_call": round(ms_step * 1e3, 2), "tflops": round(tflops, 2),
+            "hbm_frac_of_" + pk["source"]: round(value / pk["hbm_gbs"], 4),
+            "hbm_frac_of_nominal_8tbs": round(value / 8000.0, 4),
+            "tensor_frac_of_" + pk["source"]: round(tflops / pk["bf16_tflops"], 4),
+            "config": {"workload": f"{case.name}: b={case.batch}, s_q={case.s_q}, h_q={case.h_q}, h_kv={case.h_kv}, "
+                                   f"d={case.d}, dv={case.dv}, page={case.page}, causal={case.causal}, "
+                                   f"seqlens={'U' + str(case.seqlen_range) if case.seqlen_range else case.seqlens[0]}",
+                       "batch": case.batch, "s_q": case.s_q, "h_q": case.h_q, "num_parts": num_parts,
+                       "kv_bytes": fig["kv_bytes"], "bytes_per_call": fig["bytes"], "flops_per_call": fig["flops"],
+                       "l2": "no flush: KV pages touched per call exceed the 129 MB L2",
+                       "parallelism": f"replicas x{world}, one batch per GPU" if world > 1 else "single GPU"},
+            "roofline": {"bound": bound, "kernel": "split_kv", "achieved": round(achieved, 1),
+                         "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                         "peak_source": pk["source"], "split_kernel_ms": round(split_ms, 5),
+                         "traffic": traffic},
+            "clocks": clk,
+            "e2e": e2e,
+            "gpu_launches": 3 * args.steps,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def e2e_run(mla, case, x, fig, dev, stream, steps, world):
+    """Inputs from pinned host memory, outputs back to pinned host memory, every step timed."""
+    hq = x.q.cpu().pin_memory()
+    hk = x.kcache.cpu().pin_memory()
+    hbt = x.block_table.cpu().pin_memory()
+    hsl = x.cache_seqlens.cpu().pin_memory()
+    ho = torch.empty((case.batch, case.s_q, case.h_q, case.dv), dtype=torch.bfloat16).pin_memory()
+    hl = torch.empty((case.batch, case.s_q, case.h_q), dtype=torch.float32).pin_memory()
+    dq, dk = torch.empty_like(x.q), torch.empty_like(x.kcache)
+    dbt, dsl = torch.empty_like(x.block_table), torch.empty_like(x.cache_seqlens)
+
+    def one():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dbt.copy_(hbt, non_blocking=True)
+        dsl.copy_(hsl, non_blocking=True)
+        md, ns = mla.mla_get_metadata(dsl, case.num_q_rows, case.h_kv)
+        o, lse = mla.mla_decode_kvcache(dq, dk, dbt, dsl, case.dv, md, ns, softmax_scale=case.softmax_scale,
+                                        causal=case.causal)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b) / steps, world)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hbt, hsl))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hl))
+    return {"value": round(fig["bytes"] * world / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def reference_arm(args, case):
+    """This tier's reference arm: the fp64 CPU oracle, on a bounded sample per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from mla_decode_attention_latent_gb300 import workloads as W
+    x = W.make_inputs(case, device="cpu")
+    fig = workload_figures(case, x.cache_seqlens.tolist())
+    per_step = max(1.0, 120.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        time_oracle(case, x, budget_s=min(per_step, 2.0), max_seqs=1)
+    secs, call_secs, seqs, cores = [], [], 0, 1
+    for _ in range(args.steps):
+        t = time_oracle(case, x, budget_s=per_step)
+        secs.append(t["seconds"])
+        call_secs.append(t["call_seconds"])
+        seqs, cores = t["seqs"], t["cores"]
+    call = statistics.mean(call_secs)
+    value = fig["bytes"] / call / 1e9
+    line = {"metric": METRIC, "impl": "reference", "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(call * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": case.name, "batch": case.batch, "s_q": case.s_q, "h_q": case.h_q},
+            "cpu_baseline": {"kind": "oracle", "cores": cores, "value": round(value, 4), "unit": "GB/s",
+                             "sample": f"{seqs} of {case.batch} sequences per step, scaled to one call"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

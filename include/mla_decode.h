@@ -1,0 +1,199 @@
+/*
+ * mla_decode.h — C ABI of the GB300 (sm_103a) MLA decode library.
+ *
+ * Multi-head Latent Attention decoding over a paged latent KV cache.  Every
+ * query head attends to one shared latent KV head: a cached row of
+ * d = 576 bf16 values (512 latent + 64 decoupled-RoPE dims) serves as the key,
+ * and its first dv = 512 dims as the value.  Pages hold 64 tokens and are
+ * addressed through a per-sequence block table.
+ *
+ * Sources for the operations declared here:
+ *  - "Novita AI, H100 및 H200에서 FlashMLA 평가", section "MLA란 무엇인가요?",
+ *    table "MHA vs MQA vs GQA vs MLA": all heads share a compressed latent KV
+ *    vector per token, with RoPE decoupled.
+ *  - "FlashMLA란 무엇인가?" (topnet.top article 5338), section "FlashMLA의 주요
+ *    특성": bf16 and a paged KV cache with block size 64.
+ *  - same page, section "FlashMLA 설치 및 사용":
+ *      step 2 "MLA 메타데이터 가져오기": get_mla_metadata(cache_seqlens,
+ *        s_q * h_q // h_kv, h_kv) -> (tile_scheduler_metadata, num_splits),
+ *        computed once and reused by every layer;
+ *      step 3 "MLA 디코딩 실행": flash_mla_with_kvcache(q, kvcache, block_table,
+ *        cache_seqlens, dv, tile_scheduler_metadata, num_splits, causal)
+ *        -> (o, lse).
+ *  - same page, section "FlashMLA의 기술 구현" ("병렬 디코딩"): several query
+ *    tokens per step, read here as s_q > 1 with a causal mask: query i of a
+ *    sequence of length T sees cached positions < T - s_q + i + 1.
+ *
+ * Conventions for every call:
+ *  - Pointers marked "device" are CUDA device pointers on the current device;
+ *    the caller allocates, owns and frees them.  The library never allocates,
+ *    frees or retains caller memory and keeps no per-call state.
+ *  - `stream` is a CUDA stream (cudaStream_t / CUstream; NULL = legacy default).
+ *    Calls that launch work enqueue it on `stream` and return without waiting.
+ *  - Return value: MLA_OK (0) or a negative MLA_ERR_* code.  Arguments are
+ *    validated on the host before anything is launched; on an argument error
+ *    nothing is launched and no output is touched.
+ *  - bf16 tensors are raw IEEE bfloat16 bit patterns (2 bytes per element),
+ *    row-major and densely packed in the shapes given.
+ *
+ * Supported on the GPU path: d = 576, dv = 512, page size 64, h_kv = 1,
+ * any batch >= 1, any s_q >= 1 and h_q >= 1 with s_q * h_q <= 65536.
+ * Other shapes return MLA_ERR_UNSUPPORTED.
+ */
+#ifndef MLA_DECODE_H
+#define MLA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+/* status codes */
+#define MLA_OK 0
+#define MLA_ERR_INVALID_ARG (-1)   /* null pointer, negative size, inconsistent shapes */
+#define MLA_ERR_UNSUPPORTED (-2)   /* shape or device outside what the GPU path implements */
+#define MLA_ERR_WORKSPACE (-3)     /* workspace smaller than mla_workspace_bytes() */
+#define MLA_ERR_CUDA (-4)          /* a CUDA runtime call or kernel launch failed */
+#define MLA_ERR_DEVICE (-5)        /* a kernel reported an error (see mla_device_status) */
+
+/* fixed shape constants of the GPU path */
+#define MLA_PAGE_SIZE 64
+#define MLA_HEAD_DIM 576
+#define MLA_V_DIM 512
+#define MLA_METADATA_INTS 8
+/* fixed cost of one split-KV segment, in pages, used by the work partition */
+#define MLA_SCHED_FIXED_COST_PAGES 5
+
+/* device-side error bits reported through mla_device_status() */
+#define MLA_DEVERR_TIMEOUT 0x1     /* a bounded wait inside a kernel gave up */
+#define MLA_DEVERR_BLOCK_ID 0x2    /* a block_table entry was outside [0, num_blocks) */
+#define MLA_DEVERR_SEQLEN 0x4      /* a cache_seqlens entry was negative or beyond the table */
+
+/*
+ * mla_num_sm_parts — number of split-KV work parts for one decode call.
+ *
+ * Host-only query.  The caller uses it to size tile_scheduler_metadata
+ * ([num_parts * MLA_METADATA_INTS] int32) before mla_get_metadata.
+ *   device      CUDA device ordinal the decode will run on
+ *   num_q_rows  query rows per KV head: s_q * h_q / h_kv (the pages' second
+ *               argument of get_mla_metadata)
+ *   h_kv        KV heads (must be 1)
+ *   num_parts   out: number of parts (>= 1)
+ * Errors: MLA_ERR_INVALID_ARG (null out pointer, num_q_rows < 1),
+ *         MLA_ERR_UNSUPPORTED (h_kv != 1), MLA_ERR_CUDA (device query failed).
+ */
+MLA_API int mla_num_sm_parts(int device, int num_q_rows, int h_kv, int *num_parts);
+
+/*
+ * mla_get_metadata — split-KV work partition ("MLA 메타데이터 가져오기").
+ *
+ * Launches the tile-scheduler kernel on `stream`.  It reads the sequence
+ * lengths and cuts the (sequence, page) range into `num_parts` contiguous
+ * parts of near-equal cost (pages plus MLA_SCHED_FIXED_COST_PAGES per
+ * segment); a sequence may be cut across several parts (split-KV).
+ *   cache_seqlens            device int32 [batch]; entries >= 0
+ *   batch                    number of sequences (>= 1)
+ *   num_q_rows, h_kv         as for mla_num_sm_parts
+ *   num_parts                parts to produce (>= 1; normally mla_num_sm_parts)
+ *   tile_scheduler_metadata  device int32 [num_parts][MLA_METADATA_INTS], out:
+ *                            per part {begin_seq, begin_page, end_seq,
+ *                            end_page, begin_split, 0, 0, 0}; the part covers
+ *                            the (sequence, page) cursor range [begin, end)
+ *   num_splits               device int32 [batch + 1], out: prefix sum over
+ *                            sequences of the number of parts touching each
+ * The outputs stay valid for every decode call with the same cache_seqlens
+ * values, num_q_rows and num_parts (one computation serves all layers).
+ * A negative length sets MLA_DEVERR_SEQLEN in the device status word.
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED (h_kv != 1), MLA_ERR_CUDA.
+ */
+MLA_API int mla_get_metadata(const int32_t *cache_seqlens, int batch, int num_q_rows, int h_kv,
+                     int num_parts, int32_t *tile_scheduler_metadata, int32_t *num_splits,
+                     struct CUstream_st *stream);
+
+/*
+ * mla_workspace_bytes — device scratch that mla_decode_kvcache needs for the
+ * partial results of split sequences: fp32 partial outputs and their LSE for
+ * at most (batch + num_parts) splits.  Returns 0 on invalid arguments.
+ */
+MLA_API size_t mla_workspace_bytes(int batch, int s_q, int h_q, int h_kv, int dv, int num_parts);
+
+/*
+ * mla_decode_kvcache — MLA decode over the paged latent cache ("MLA 디코딩 실행").
+ *
+ * For batch b, query token i, head h (all heads share KV head 0):
+ *   T    = cache_seqlens[b]                 (causal == 0, or s_q == 1)
+ *   T    = cache_seqlens[b] - s_q + i + 1   (causal != 0)
+ *   k_j  = kcache[block_table[b][j / 64]][j % 64][0][0..576),   j < T
+ *   s_j  = softmax_scale * <q[b][i][h], k_j>
+ *   lse  = ln sum_j exp(s_j)
+ *   o    = sum_j exp(s_j - lse) * k_j[0..512)
+ * Rows with T <= 0 get o = 0 and lse = -inf.
+ *
+ *   q              device bf16 [batch][s_q][h_q][d]
+ *   kcache         device bf16 [num_blocks][64][h_kv][d]; 16-byte aligned.
+ *                  Rows past a sequence's end may hold any bits (NaN too).
+ *   num_blocks     physical pages in kcache
+ *   block_table    device int32 [batch][max_blocks_per_seq]; the first
+ *                  ceil(T_b / 64) entries of row b must lie in [0, num_blocks)
+ *   cache_seqlens  device int32 [batch]; 0 <= T_b <= 64 * max_blocks_per_seq
+ *   d, dv          576 and 512
+ *   tile_scheduler_metadata, num_splits, num_parts
+ *                  from mla_get_metadata with the same cache_seqlens
+ *   softmax_scale  multiplies q.k before the softmax (e.g. 1/sqrt(576))
+ *   causal         nonzero: the causal rule above (only matters for s_q > 1)
+ *   o              device bf16 [batch][s_q][h_q][dv], out
+ *   lse            device fp32 [batch][s_q][h_q], out (natural log)
+ *   workspace      device scratch of at least mla_workspace_bytes(...) bytes,
+ *                  256-byte aligned; its contents on entry do not matter
+ * Out-of-range block ids or lengths found on the device are skipped and set
+ * bits in the device status word (mla_device_status); they never fault.
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_WORKSPACE,
+ *         MLA_ERR_CUDA (launch failure).
+ */
+MLA_API int mla_decode_kvcache(const void *q, const void *kcache, int64_t num_blocks,
+                       const int32_t *block_table, int max_blocks_per_seq,
+                       const int32_t *cache_seqlens, int batch, int s_q, int h_q, int h_kv,
+                       int d, int dv, const int32_t *tile_scheduler_metadata,
+                       const int32_t *num_splits, int num_parts, float softmax_scale,
+                       int causal, void *o, float *lse, void *workspace,
+                       size_t workspace_bytes, struct CUstream_st *stream);
+
+/*
+ * mla_device_status — read the device status word of the current device.
+ *
+ * Synchronizes the device, stores the OR of the MLA_DEVERR_* bits raised by
+ * kernels since the last clear into *status, and clears the word if `clear`
+ * is nonzero.  Returns MLA_OK, MLA_ERR_INVALID_ARG or MLA_ERR_CUDA.
+ */
+MLA_API int mla_device_status(int *status, int clear);
+
+/*
+ * mla_set_timing_events — profiling aid: time the split-KV kernel alone.
+ *
+ * While set, every mla_decode_kvcache call records `split_begin` on its
+ * stream just before the split-KV kernel and `split_end` just after it, so
+ * that cudaEventElapsedTime gives that kernel's duration (the combine kernel
+ * is outside the pair).  Both are cudaEvent_t handles created by the caller
+ * on the device the decode runs on; pass NULL, NULL to stop.  The setting is
+ * process-wide.  Returns MLA_OK, or MLA_ERR_INVALID_ARG if only one is NULL.
+ */
+MLA_API int mla_set_timing_events(void *split_begin, void *split_end);
+
+/* mla_status_string — static description of a status code (never NULL). */
+MLA_API const char *mla_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H */

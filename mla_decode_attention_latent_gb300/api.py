@@ -1,0 +1,138 @@
+"""Python binding of the MLA decode C ABI (argument marshalling only).
+
+The two calls mirror the usage page "FlashMLA란 무엇인가?" (section "FlashMLA
+설치 및 사용", steps 2 and 3):
+
+    md, ns = mla_get_metadata(cache_seqlens, s_q * h_q // h_kv, h_kv)
+    for layer in range(num_layers):
+        o, lse = mla_decode_kvcache(q[layer], kcache[layer], block_table, cache_seqlens,
+                                    dv, md, ns, causal=True)
+
+``get_mla_metadata`` and ``flash_mla_with_kvcache`` are the same calls under
+the page's names.  Every step runs in the CUDA library; this module only
+checks tensor properties, allocates outputs with torch on the caller's device
+and passes raw pointers and the current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Optional, Tuple
+
+import torch
+
+from . import _lib
+from ._lib import MLA_METADATA_INTS, MLA_V_DIM, check, load
+
+
+def _stream_handle(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _need_cuda(name: str, t: torch.Tensor, dtype: torch.dtype) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def mla_num_sm_parts(num_q_rows: int, h_kv: int = 1, device: Optional[torch.device] = None) -> int:
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    out = ctypes.c_int(0)
+    check("mla_num_sm_parts", load().mla_num_sm_parts(dev.index or 0, int(num_q_rows), int(h_kv), ctypes.byref(out)))
+    return out.value
+
+
+def mla_get_metadata(cache_seqlens: torch.Tensor, num_q_rows: int, h_kv: int = 1,
+                     num_parts: Optional[int] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Split-KV work partition: (tile_scheduler_metadata int32 [P, 8], num_splits int32 [b + 1])."""
+    _need_cuda("cache_seqlens", cache_seqlens, torch.int32)
+    dev = cache_seqlens.device
+    if num_parts is None:
+        num_parts = mla_num_sm_parts(num_q_rows, h_kv, dev)
+    batch = cache_seqlens.numel()
+    md = torch.empty((num_parts, MLA_METADATA_INTS), dtype=torch.int32, device=dev)
+    ns = torch.empty((batch + 1,), dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        st = load().mla_get_metadata(cache_seqlens.data_ptr(), batch, int(num_q_rows), int(h_kv), int(num_parts),
+                                     md.data_ptr(), ns.data_ptr(), _stream_handle(dev))
+    check("mla_get_metadata", st)
+    return md, ns
+
+
+def mla_workspace_bytes(batch: int, s_q: int, h_q: int, h_kv: int, dv: int, num_parts: int) -> int:
+    n = load().mla_workspace_bytes(batch, s_q, h_q, h_kv, dv, num_parts)
+    if n == 0:
+        raise ValueError("invalid shape for the decode workspace")
+    return int(n)
+
+
+def mla_decode_kvcache(q: torch.Tensor, kcache: torch.Tensor, block_table: torch.Tensor,
+                       cache_seqlens: torch.Tensor, dv: int, tile_scheduler_metadata: torch.Tensor,
+                       num_splits: torch.Tensor, softmax_scale: Optional[float] = None, causal: bool = False,
+                       out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """MLA decode: returns (o bf16 [b, s_q, h_q, dv], lse fp32 [b, s_q, h_q])."""
+    _need_cuda("q", q, torch.bfloat16)
+    _need_cuda("kcache", kcache, torch.bfloat16)
+    _need_cuda("block_table", block_table, torch.int32)
+    _need_cuda("cache_seqlens", cache_seqlens, torch.int32)
+    _need_cuda("tile_scheduler_metadata", tile_scheduler_metadata, torch.int32)
+    _need_cuda("num_splits", num_splits, torch.int32)
+    if q.dim() != 4 or kcache.dim() != 4 or block_table.dim() != 2:
+        raise ValueError("q must be [b, s_q, h_q, d], kcache [num_blocks, page, h_kv, d], block_table [b, max_blocks]")
+    b, s_q, h_q, d = q.shape
+    num_blocks, page, h_kv, dk = kcache.shape
+    if dk != d or page != _lib.MLA_PAGE_SIZE:
+        raise ValueError("kcache must be [num_blocks, 64, h_kv, d] with the same d as q")
+    if block_table.shape[0] != b or cache_seqlens.numel() != b or num_splits.numel() != b + 1:
+        raise ValueError("batch size differs between q, block_table, cache_seqlens and num_splits")
+    if tile_scheduler_metadata.dim() != 2 or tile_scheduler_metadata.shape[1] != MLA_METADATA_INTS:
+        raise ValueError("tile_scheduler_metadata must be [num_parts, 8]")
+    num_parts = tile_scheduler_metadata.shape[0]
+    dev = q.device
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((b, s_q, h_q, dv), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((b, s_q, h_q), dtype=torch.float32, device=dev)
+    _need_cuda("out", out, torch.bfloat16)
+    _need_cuda("lse", lse, torch.float32)
+    if tuple(out.shape) != (b, s_q, h_q, dv) or tuple(lse.shape) != (b, s_q, h_q):
+        raise ValueError("out must be [b, s_q, h_q, dv] and lse [b, s_q, h_q]")
+    ws_need = mla_workspace_bytes(b, s_q, h_q, h_kv, dv, num_parts) if dv == MLA_V_DIM and h_q % h_kv == 0 else 256
+    if workspace is None:
+        workspace = torch.empty((ws_need,), dtype=torch.uint8, device=dev)
+    _need_cuda("workspace", workspace, torch.uint8)
+    with torch.cuda.device(dev):
+        st = load().mla_decode_kvcache(
+            q.data_ptr(), kcache.data_ptr(), num_blocks, block_table.data_ptr(), block_table.shape[1],
+            cache_seqlens.data_ptr(), b, s_q, h_q, h_kv, d, dv, tile_scheduler_metadata.data_ptr(),
+            num_splits.data_ptr(), num_parts, float(softmax_scale), int(bool(causal)), out.data_ptr(),
+            lse.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream_handle(dev))
+    check("mla_decode_kvcache", st)
+    return out, lse
+
+
+def mla_device_status(clear: bool = True) -> int:
+    """Synchronize and return the OR of the MLA_DEVERR_* bits kernels raised."""
+    v = ctypes.c_int(0)
+    check("mla_device_status", load().mla_device_status(ctypes.byref(v), int(bool(clear))))
+    return v.value
+
+
+def mla_set_timing_events(split_begin: Optional[torch.cuda.Event], split_end: Optional[torch.cuda.Event]) -> None:
+    """Record the two events around the split-KV kernel of every later decode call (None, None: stop)."""
+    b = split_begin.cuda_event if split_begin is not None else None
+    e = split_end.cuda_event if split_end is not None else None
+    check("mla_set_timing_events", load().mla_set_timing_events(b, e))
+
+
+# the usage page's names for the same two calls
+get_mla_metadata = mla_get_metadata
+flash_mla_with_kvcache = mla_decode_kvcache

@@ -1,0 +1,187 @@
+// C ABI of the MLA decode library: argument validation, workspace layout and
+// kernel launches.  See include/mla_decode.h for the contract of each call.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "mla_internal.h"
+
+namespace mla {
+namespace {
+
+// Device status word: kernels OR MLA_DEVERR_* bits into it instead of
+// trapping.  Host code reaches it through its per-device address.
+__device__ unsigned int g_status_word;
+
+constexpr int kMaxDevices = 64;
+unsigned int *g_status_addr[kMaxDevices] = {};
+std::mutex g_status_mutex;
+
+int status_address(unsigned int **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_status_mutex);
+    if (!g_status_addr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) return MLA_ERR_CUDA;
+        g_status_addr[dev] = static_cast<unsigned int *>(ptr);
+    }
+    *out = g_status_addr[dev];
+    return MLA_OK;
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kRowsPerTile = 128;  // query rows per tensor-core tile
+
+std::mutex g_timing_mutex;
+cudaEvent_t g_split_begin = nullptr, g_split_end = nullptr;
+constexpr int kMaxRows = 65536;
+
+}  // namespace
+
+size_t workspace_bytes(int batch, int rows, int num_parts) {
+    const size_t splits = (size_t)batch + (size_t)num_parts;
+    return align_up(splits * rows * kDv * sizeof(float)) + align_up(splits * rows * sizeof(float));
+}
+
+void carve_workspace(void *ws, int batch, int rows, int num_parts, float **o_accum, float **lse_accum) {
+    const size_t splits = (size_t)batch + (size_t)num_parts;
+    char *base = static_cast<char *>(ws);
+    *o_accum = reinterpret_cast<float *>(base);
+    *lse_accum = reinterpret_cast<float *>(base + align_up(splits * rows * kDv * sizeof(float)));
+}
+
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+int mla_num_sm_parts(int device, int num_q_rows, int h_kv, int *num_parts) {
+    if (!num_parts || num_q_rows < 1 || h_kv < 1) return MLA_ERR_INVALID_ARG;
+    if (h_kv != 1) return MLA_ERR_UNSUPPORTED;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return MLA_ERR_CUDA;
+    const int pairs = sms / 2 > 0 ? sms / 2 : 1;  // one CTA pair (2 SMs) per part and row tile
+    const int tiles = (num_q_rows + kRowsPerTile - 1) / kRowsPerTile;
+    const int parts = pairs / tiles;
+    *num_parts = parts > 0 ? parts : 1;
+    return MLA_OK;
+}
+
+int mla_get_metadata(const int32_t *cache_seqlens, int batch, int num_q_rows, int h_kv, int num_parts,
+                     int32_t *tile_scheduler_metadata, int32_t *num_splits, struct CUstream_st *stream) {
+    if (!cache_seqlens || !tile_scheduler_metadata || !num_splits) return MLA_ERR_INVALID_ARG;
+    if (batch < 1 || num_q_rows < 1 || h_kv < 1 || num_parts < 1) return MLA_ERR_INVALID_ARG;
+    if (h_kv != 1) return MLA_ERR_UNSUPPORTED;
+    unsigned int *status = nullptr;
+    if (status_address(&status) != MLA_OK) return MLA_ERR_CUDA;
+    cudaError_t e = launch_schedule(cache_seqlens, batch, num_parts, tile_scheduler_metadata, num_splits, status,
+                                    reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+size_t mla_workspace_bytes(int batch, int s_q, int h_q, int h_kv, int dv, int num_parts) {
+    if (batch < 1 || s_q < 1 || h_q < 1 || h_kv < 1 || num_parts < 1 || dv != kDv) return 0;
+    if (h_q % h_kv) return 0;
+    const long long rows = (long long)s_q * h_q / h_kv;
+    if (rows > kMaxRows) return 0;
+    return workspace_bytes(batch, (int)rows, num_parts);
+}
+
+int mla_decode_kvcache(const void *q, const void *kcache, int64_t num_blocks, const int32_t *block_table,
+                       int max_blocks_per_seq, const int32_t *cache_seqlens, int batch, int s_q, int h_q,
+                       int h_kv, int d, int dv, const int32_t *tile_scheduler_metadata,
+                       const int32_t *num_splits, int num_parts, float softmax_scale, int causal, void *o,
+                       float *lse, void *workspace, size_t ws_bytes, struct CUstream_st *stream) {
+    if (!q || !kcache || !block_table || !cache_seqlens || !tile_scheduler_metadata || !num_splits || !o || !lse ||
+        !workspace)
+        return MLA_ERR_INVALID_ARG;
+    if (batch < 1 || batch > 65535 || s_q < 1 || h_q < 1 || h_kv < 1 || num_blocks < 1 ||
+        max_blocks_per_seq < 1 || num_parts < 1 || d < 1 || dv < 1)
+        return MLA_ERR_INVALID_ARG;
+    if (!(softmax_scale == softmax_scale)) return MLA_ERR_INVALID_ARG;
+    if (d != kDqk || dv != kDv || h_kv != 1) return MLA_ERR_UNSUPPORTED;
+    if ((long long)s_q * h_q > kMaxRows) return MLA_ERR_UNSUPPORTED;
+    if ((long long)max_blocks_per_seq * kPage > 0x7fffffffLL) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(kcache) || !aligned16(o) || !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
+    const int rows = s_q * h_q;
+    if (ws_bytes < workspace_bytes(batch, rows, num_parts)) return MLA_ERR_WORKSPACE;
+
+    DecodeParams p{};
+    p.q = static_cast<const uint16_t *>(q);
+    p.kcache = static_cast<const uint16_t *>(kcache);
+    p.num_blocks = num_blocks;
+    p.block_table = block_table;
+    p.max_blocks = max_blocks_per_seq;
+    p.seqlens = cache_seqlens;
+    p.batch = batch;
+    p.s_q = s_q;
+    p.h_q = h_q;
+    p.rows = rows;
+    p.metadata = tile_scheduler_metadata;
+    p.num_splits = num_splits;
+    p.num_parts = num_parts;
+    p.max_splits = batch + num_parts;
+    p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.causal = (causal != 0 && s_q > 1) ? 1 : 0;
+    p.o = static_cast<uint16_t *>(o);
+    p.lse = lse;
+    carve_workspace(workspace, batch, rows, num_parts, &p.o_accum, &p.lse_accum);
+    if (status_address(&p.status) != MLA_OK) return MLA_ERR_CUDA;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaEvent_t ev_begin, ev_end;
+    {
+        std::lock_guard<std::mutex> lock(g_timing_mutex);
+        ev_begin = g_split_begin;
+        ev_end = g_split_end;
+    }
+    if (ev_begin && cudaEventRecord(ev_begin, s) != cudaSuccess) return MLA_ERR_CUDA;
+    cudaError_t e = launch_split_kv_simt(p, s);
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
+    if (ev_end && cudaEventRecord(ev_end, s) != cudaSuccess) return MLA_ERR_CUDA;
+    e = launch_combine(p, s);
+    return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_device_status(int *status, int clear) {
+    if (!status) return MLA_ERR_INVALID_ARG;
+    unsigned int *addr = nullptr;
+    if (status_address(&addr) != MLA_OK) return MLA_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return MLA_ERR_CUDA;
+    unsigned int v = 0;
+    if (cudaMemcpy(&v, addr, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
+    if (clear && v) {
+        const unsigned int zero = 0;
+        if (cudaMemcpy(addr, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return MLA_ERR_CUDA;
+    }
+    *status = (int)v;
+    return MLA_OK;
+}
+
+int mla_set_timing_events(void *split_begin, void *split_end) {
+    if ((split_begin == nullptr) != (split_end == nullptr)) return MLA_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_timing_mutex);
+    g_split_begin = static_cast<cudaEvent_t>(split_begin);
+    g_split_end = static_cast<cudaEvent_t>(split_end);
+    return MLA_OK;
+}
+
+const char *mla_status_string(int status) {
+    switch (status) {
+        case MLA_OK: return "ok";
+        case MLA_ERR_INVALID_ARG: return "invalid argument";
+        case MLA_ERR_UNSUPPORTED: return "unsupported shape or device";
+        case MLA_ERR_WORKSPACE: return "workspace too small";
+        case MLA_ERR_CUDA: return "CUDA runtime error";
+        case MLA_ERR_DEVICE: return "a kernel reported a device-side error";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

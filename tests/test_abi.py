@@ -1,0 +1,114 @@
+"""The C ABI library on the host: it loads, exports every declared call, and
+rejects bad arguments before touching the GPU (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mla_decode_attention_latent_gb300 as mla
+from mla_decode_attention_latent_gb300 import _lib
+from mla_decode_attention_latent_gb300 import build as cuda_build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "mla_decode.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()
+    return _lib.load()
+
+
+def declared_calls():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"MLA_API\s+[\w\s\*]*?\b(mla_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_calls():
+    assert declared_calls() == sorted(_lib.SIGNATURES)
+
+
+def test_library_exports_every_declared_call(lib):
+    for name in declared_calls():
+        assert hasattr(lib, name), name
+
+
+def test_header_constants_match_binding():
+    text = open(HEADER).read()
+    for name in ("MLA_OK", "MLA_ERR_INVALID_ARG", "MLA_ERR_UNSUPPORTED", "MLA_ERR_WORKSPACE", "MLA_ERR_CUDA",
+                 "MLA_ERR_DEVICE", "MLA_PAGE_SIZE", "MLA_HEAD_DIM", "MLA_V_DIM", "MLA_METADATA_INTS",
+                 "MLA_DEVERR_TIMEOUT", "MLA_DEVERR_BLOCK_ID", "MLA_DEVERR_SEQLEN"):
+        m = re.search(rf"#define {name} \(?(-?0x[0-9a-fA-F]+|-?\d+)\)?", text)
+        assert m, name
+        assert int(m.group(1), 0) == getattr(_lib, name), name
+
+
+def test_fixed_cost_matches_oracle_partition():
+    import oracle
+    m = re.search(r"#define MLA_SCHED_FIXED_COST_PAGES (\d+)", open(HEADER).read())
+    assert int(m.group(1)) == oracle.SCHED_FIXED_COST_PAGES
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, 7):
+        assert isinstance(lib.mla_status_string(code), bytes)
+    assert lib.mla_status_string(-3) == b"workspace too small"
+
+
+def test_workspace_bytes(lib):
+    n = lib.mla_workspace_bytes(64, 1, 128, 1, 512, 76)
+    splits, rows = 64 + 76, 128
+    assert n >= splits * rows * 512 * 4 + splits * rows * 4
+    assert n % 256 == 0
+    assert lib.mla_workspace_bytes(0, 1, 128, 1, 512, 76) == 0
+    assert lib.mla_workspace_bytes(4, 1, 128, 1, 256, 76) == 0
+    assert lib.mla_workspace_bytes(4, 1, 127, 2, 512, 76) == 0
+
+
+def _decode(lib, **over):
+    a = dict(q=16, kcache=16, num_blocks=4, bt=16, max_blocks=2, sl=16, batch=2, s_q=1, h_q=16, h_kv=1, d=576,
+             dv=512, md=16, ns=16, num_parts=3, scale=1 / 24, causal=0, o=16, lse=16, ws=256, ws_bytes=1 << 30)
+    a.update(over)
+    return lib.mla_decode_kvcache(a["q"], a["kcache"], a["num_blocks"], a["bt"], a["max_blocks"], a["sl"],
+                                  a["batch"], a["s_q"], a["h_q"], a["h_kv"], a["d"], a["dv"], a["md"], a["ns"],
+                                  a["num_parts"], a["scale"], a["causal"], a["o"], a["lse"], a["ws"],
+                                  a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), _lib.MLA_ERR_INVALID_ARG),
+    (dict(kcache=None), _lib.MLA_ERR_INVALID_ARG),
+    (dict(ws=None), _lib.MLA_ERR_INVALID_ARG),
+    (dict(batch=0), _lib.MLA_ERR_INVALID_ARG),
+    (dict(num_parts=0), _lib.MLA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), _lib.MLA_ERR_INVALID_ARG),
+    (dict(d=512), _lib.MLA_ERR_UNSUPPORTED),
+    (dict(dv=256), _lib.MLA_ERR_UNSUPPORTED),
+    (dict(h_kv=2, h_q=16), _lib.MLA_ERR_UNSUPPORTED),
+    (dict(s_q=1024, h_q=128), _lib.MLA_ERR_UNSUPPORTED),
+    (dict(q=24), _lib.MLA_ERR_INVALID_ARG),            # not 16-byte aligned
+    (dict(ws_bytes=1024), _lib.MLA_ERR_WORKSPACE),
+])
+def test_decode_rejects_bad_arguments_before_launch(lib, over, code):
+    assert _decode(lib, **over) == code
+
+
+def test_metadata_rejects_bad_arguments(lib):
+    assert lib.mla_get_metadata(None, 2, 16, 1, 3, 16, 16, None) == _lib.MLA_ERR_INVALID_ARG
+    assert lib.mla_get_metadata(16, 0, 16, 1, 3, 16, 16, None) == _lib.MLA_ERR_INVALID_ARG
+    assert lib.mla_get_metadata(16, 2, 16, 2, 3, 16, 16, None) == _lib.MLA_ERR_UNSUPPORTED
+    assert lib.mla_get_metadata(16, 2, 16, 1, 0, 16, 16, None) == _lib.MLA_ERR_INVALID_ARG
+
+
+def test_num_sm_parts_rejects_bad_arguments(lib):
+    out = ctypes.c_int(0)
+    assert lib.mla_num_sm_parts(0, 0, 1, ctypes.byref(out)) == _lib.MLA_ERR_INVALID_ARG
+    assert lib.mla_num_sm_parts(0, 128, 2, ctypes.byref(out)) == _lib.MLA_ERR_UNSUPPORTED
+    assert lib.mla_num_sm_parts(0, 128, 1, None) == _lib.MLA_ERR_INVALID_ARG
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros(4, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        mla.mla_get_metadata(x, 16, 1, num_parts=3)

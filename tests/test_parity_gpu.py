@@ -1,0 +1,147 @@
+"""CUDA path vs the fp64 oracle, through the C ABI (GPU only).
+
+Small cases are compared element by element on every output; the full-size
+workloads (launched exactly as the benchmark launches them) are compared on
+sampled rows that the oracle computes one by one.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mla_decode_attention_latent_gb300 import _lib
+from mla_decode_attention_latent_gb300 import workloads as W
+from tests.parity import assert_parity, oracle_of, run_gpu, sampled_oracle, to_device
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0)
+
+
+def case(name, batch, s_q, h_q, seqlens, causal=False, seed=100, pool_pages=None):
+    return W.Case(name, batch=batch, s_q=s_q, h_q=h_q, seqlens=tuple(seqlens), causal=causal, seed=seed,
+                  pool_pages=pool_pages)
+
+
+def check(c, num_parts=None, mutate=None):
+    x = W.make_inputs(c, "cpu")
+    if mutate is not None:
+        mutate(x)
+    o_ref, lse_ref = oracle_of(x)
+    o, lse, md, ns, st = run_gpu(to_device(x, DEV), num_parts=num_parts)
+    assert st == 0, f"device status {st:#x}"
+    assert_parity(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, c.name)
+    return o, lse
+
+
+def test_tiny_config():
+    check(W.TINY)
+
+
+@pytest.mark.parametrize("num_parts", [1, 2, 3, 7, None])
+def test_split_counts(num_parts):
+    # several row tiles' worth of work, a ragged last page, splits forced by num_parts
+    c = case("splits", 3, 1, 128, [1000, 77, 2100], seed=101)
+    check(c, num_parts=num_parts)
+
+
+def test_split_invariance():
+    c = case("split-inv", 2, 1, 128, [3000, 1500], seed=102)
+    x = to_device(W.make_inputs(c, "cpu"), DEV)
+    o1, l1, *_ = run_gpu(x, num_parts=1)
+    for p in (2, 5, 40):
+        o2, l2, *_ = run_gpu(x, num_parts=p)
+        assert torch.allclose(o1.float(), o2.float(), rtol=1e-2, atol=2e-3)
+        assert torch.allclose(l1, l2, atol=1e-4)
+
+
+@pytest.mark.parametrize("h_q", [16, 32, 64, 128])
+def test_head_counts(h_q):
+    check(case(f"h{h_q}", 2, 1, h_q, [700, 129], seed=103))
+
+
+@pytest.mark.parametrize("s_q,causal", [(2, True), (3, False), (8, True)])
+def test_multi_token(s_q, causal):
+    check(case(f"mtp{s_q}", 2, s_q, 128 if s_q < 8 else 32, [513, 70], causal=causal, seed=104))
+
+
+def test_ragged_row_tile():
+    # 3 * 20 = 60 query rows: a partial row tile
+    check(case("ragged-rows", 2, 3, 20, [300, 65], causal=True, seed=105))
+
+
+@pytest.mark.parametrize("seqlens", [[0, 5], [1, 64], [63, 65], [128, 0, 1]])
+def test_edge_lengths(seqlens):
+    check(case("edge", len(seqlens), 1, 32, seqlens, seed=106))
+
+
+def test_causal_shorter_than_tokens():
+    # s_q = 4 > seqlen for the first sequence: its first rows see no key
+    check(case("causal-short", 2, 4, 16, [2, 90], causal=True, seed=107))
+
+
+def test_nan_garbage_past_the_end():
+    def poison(x):
+        sl = x.cache_seqlens.tolist()
+        bt = x.block_table
+        used = set()
+        for b, t in enumerate(sl):
+            n = (t + 63) // 64
+            used.update(bt[b, :n].tolist())
+            if t % 64:
+                x.kcache[bt[b, n - 1], t % 64:] = float("nan")
+        for p in range(x.kcache.shape[0]):
+            if p not in used:
+                x.kcache[p] = float("nan")
+    c = case("nan-tail", 3, 2, 64, [100, 37, 250], causal=True, seed=108, pool_pages=12)
+    check(c, mutate=poison)
+
+
+def test_bad_block_id_is_reported_not_faulted():
+    import mla_decode_attention_latent_gb300 as mla
+    c = case("bad-block", 2, 1, 16, [100, 37], seed=109)
+    x = to_device(W.make_inputs(c, "cpu"), DEV)
+    x.block_table[0, 1] = 10_000_000   # outside the pool
+    mla.mla_device_status(clear=True)
+    _, _, _, _, st = run_gpu(x)
+    assert st & _lib.MLA_DEVERR_BLOCK_ID
+
+
+def test_scheduler_matches_oracle_partition():
+    import mla_decode_attention_latent_gb300 as mla
+    rng = np.random.default_rng(7)
+    for trial in range(20):
+        batch = int(rng.integers(1, 300))
+        sl = rng.integers(0, 20000, size=batch).astype(np.int32)
+        parts = int(rng.integers(1, 200))
+        md, ns = mla.mla_get_metadata(torch.from_numpy(sl).to(DEV), 128, 1, num_parts=parts)
+        md_ref, ns_ref = oracle.schedule(sl, parts)
+        assert np.array_equal(md.cpu().numpy(), md_ref), trial
+        assert np.array_equal(ns.cpu().numpy(), ns_ref), trial
+
+
+def test_deterministic():
+    c = case("det", 2, 1, 128, [2000, 900], seed=110)
+    x = to_device(W.make_inputs(c, "cpu"), DEV)
+    o1, l1, *_ = run_gpu(x)
+    o2, l2, *_ = run_gpu(x)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("name", ["uniform", "variable", "mtp", "long"])
+def test_full_size_sampled(name):
+    c = W.CASES[name]
+    x = W.make_inputs(c, device="cuda")
+    o, lse, _, _, st = run_gpu(x)
+    assert st == 0, f"device status {st:#x}"
+    rng = np.random.default_rng(123)
+    seqs = sorted(rng.choice(c.batch, size=min(6, c.batch), replace=False).tolist())
+    rows, o_ref, lse_ref = sampled_oracle(x, seqs, rows_per_seq=12, rng=rng)
+    o_gpu = o.reshape(-1, c.dv)[torch.from_numpy(rows).to(DEV)].float().cpu().numpy()
+    lse_gpu = lse.reshape(-1)[torch.from_numpy(rows).to(DEV)].cpu().numpy()
+    assert_parity(o_gpu, lse_gpu, o_ref, lse_ref, name)
+    # properties that hold on every row: finite outputs, LSE >= the largest score's share
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    del x, o, lse
+    torch.cuda.empty_cache()
