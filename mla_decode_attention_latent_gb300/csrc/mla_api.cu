@@ -64,9 +64,15 @@ extern "C" {
 int mla_num_sm_parts(int device, int num_q_rows, int h_kv, int *num_parts) {
     if (!num_parts || num_q_rows < 1 || h_kv < 1) return MLA_ERR_INVALID_ARG;
     if (h_kv != 1) return MLA_ERR_UNSUPPORTED;
-    int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return MLA_ERR_CUDA;
-    const int pairs = sms / 2 > 0 ? sms / 2 : 1;  // one CTA pair (2 SMs) per part and row tile
+    int prev = 0;
+    if (cudaGetDevice(&prev) != cudaSuccess) return MLA_ERR_CUDA;
+    if (device != prev && cudaSetDevice(device) != cudaSuccess) return MLA_ERR_CUDA;
+    // one CTA pair (two SMs) per part and row tile: as many pairs as fit at once
+    int pairs = 0;
+    cudaError_t e = split_kv_tc_max_pairs(&pairs);
+    if (device != prev) cudaSetDevice(prev);
+    if (e != cudaSuccess) return MLA_ERR_CUDA;
+    if (pairs < 1) pairs = 1;
     const int tiles = (num_q_rows + kRowsPerTile - 1) / kRowsPerTile;
     const int parts = pairs / tiles;
     *num_parts = parts > 0 ? parts : 1;
@@ -142,7 +148,7 @@ int mla_decode_kvcache(const void *q, const void *kcache, int64_t num_blocks, co
         ev_end = g_split_end;
     }
     if (ev_begin && cudaEventRecord(ev_begin, s) != cudaSuccess) return MLA_ERR_CUDA;
-    cudaError_t e = launch_split_kv_simt(p, s);
+    cudaError_t e = launch_split_kv_tc(p, s);
     if (e != cudaSuccess) return MLA_ERR_CUDA;
     if (ev_end && cudaEventRecord(ev_end, s) != cudaSuccess) return MLA_ERR_CUDA;
     e = launch_combine(p, s);

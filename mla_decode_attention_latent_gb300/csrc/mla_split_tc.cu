@@ -1,0 +1,674 @@
+// Split-KV MLA decode on sm_103a tensor cores: one CTA pair per (part, row tile).
+//
+// What is computed (per query row r = i * h_q + h of sequence b, over the keys
+// of the part's page range; see include/mla_decode.h):
+//   s_j = scale * <q_r, k_j>,  p_j = 2^(s_j log2 e - m),  O = sum_j p_j v_j / l
+// with an fp32 online softmax (running max m, running sum l), and at the end
+// of the range either the final O (bf16) and LSE, or an fp32 partial O and
+// partial LSE for the combine kernel when the sequence is split.  Sources:
+// "FlashMLA란 무엇인가?" (topnet.top article 5338), sections "FlashMLA의 주요
+// 특성" (bf16, paged cache, block 64) and "FlashMLA 설치 및 사용" step 3 (the
+// decode call returns o and lse); "Novita AI, H100 및 H200에서 FlashMLA 평가",
+// table "MHA vs MQA vs GQA vs MLA" (every head shares the latent KV row, so
+// QK^T and PV are dense contractions over all heads of a tile).
+//
+// Design (GB300-first; the pages' kernel is a Hopper design and only prior art):
+// a 128 x 512 fp32 output accumulator fills a whole SM's tensor memory, so the
+// work of one tile is split across the two CTAs of a cluster by role:
+//
+//   score CTA (rank 0)                     value CTA (rank 1)
+//   ------------------                     ------------------
+//   Q tile [128 x 576] bf16 in TMEM        O tile [128 x 512] fp32 in TMEM
+//   TMA: page -> 9 swizzled K chunks       TMA: page -> 8 swizzled V chunks
+//   tcgen05 S = Q K^T  (ts, N = 64)        tcgen05 O += P V  (ss, N = 2 x 256)
+//   4 warps: mask + online softmax,        4 warps: zero the invalid tail rows
+//     P (bf16) and the per-row O              of V, rescale O rows when the
+//     rescale factor -> peer's smem           running max moved, epilogue
+//
+// Both CTAs read each page from global memory (the second read normally hits
+// L2).  P travels through distributed shared memory (16 KB per page); the
+// value CTA's MMA commit releases the P buffer back to the score CTA through
+// a multicast commit.  The running max is rescaled lazily: O is only
+// corrected when a page's maximum exceeds the current one by more than 2^8.
+//
+// Warp roles (192 threads): warp 0 issues TMA, warp 1 allocates TMEM and
+// issues MMAs (one elected lane), warps 2..5 are the row warps; thread t of
+// warp w owns TMEM lane / tile row 32 * (w % 4) + t.
+//
+// Every wait is bounded (mla_sm103.cuh); on a timeout the kernel raises
+// MLA_DEVERR_TIMEOUT, tells its peer CTA to stop, and unwinds.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include <mutex>
+
+#include "mla_internal.h"
+#include "mla_sm103.cuh"
+
+namespace mla {
+namespace {
+
+using namespace sm103;
+
+constexpr int kThreads = 192;
+constexpr int kTileRows = 128;                 // query rows per tile = TMEM lanes
+constexpr int kKStages = 3;                    // K ring (score CTA)
+constexpr int kVStages = 2;                    // V ring (value CTA)
+constexpr int kSBufs = 3;                      // S buffers in TMEM (score CTA)
+constexpr int kPBufs = 2;                      // P buffers in the value CTA's smem
+constexpr int kKChunks = kDqk / 64;            // 9 chunks of 64 dims (128 B rows)
+constexpr int kVChunks = kDv / 64;             // 8
+constexpr uint32_t kChunkBytes = kPage * 128;  // 64 tokens x 128 B = 8 KB
+constexpr uint32_t kKStageBytes = kKChunks * kChunkBytes;  // 72 KB
+constexpr uint32_t kVStageBytes = kVChunks * kChunkBytes;  // 64 KB
+constexpr uint32_t kPBytes = kTileRows * 128;             // 16 KB: 128 rows x 64 bf16
+constexpr uint32_t kQCols = kDqk / 2;                      // Q: 288 TMEM columns of bf16 pairs
+constexpr uint32_t kSCol0 = kQCols;                        // S buffers follow Q
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (log2 units)
+
+// shared-memory layout (offsets from the 1024-byte aligned base); both CTAs
+// use the same offsets so that peer addresses are plain mapa() translations
+constexpr uint32_t kRingOff = 0;
+constexpr uint32_t kRingBytes = kKStages * kKStageBytes;                 // 216 KB
+constexpr uint32_t kPBufOff = kVStages * kVStageBytes;                   // value CTA: after its V ring
+constexpr uint32_t kMsgOff = kPBufOff + kPBufs * kPBytes;                // value CTA: per-page row data
+constexpr uint32_t kMsgBytes = 2 * kTileRows * sizeof(float);            // fac[128], inv_l[128]
+static_assert(kMsgOff + kPBufs * kMsgBytes <= kRingBytes, "value CTA buffers must fit the ring region");
+constexpr uint32_t kBarOff = kRingBytes;
+
+enum Bar {
+    // score CTA
+    B_KFULL = 0, B_KEMPTY = B_KFULL + kKStages, B_SFULL = B_KEMPTY + kKStages, B_SEMPTY = B_SFULL + kSBufs,
+    B_QFULL = B_SEMPTY + kSBufs, B_PFREE = B_QFULL + 1,
+    // value CTA
+    B_VFULL = B_PFREE + kPBufs, B_VEMPTY = B_VFULL + kVStages, B_PFULL = B_VEMPTY + kVStages,
+    B_PREADY = B_PFULL + kPBufs, B_PVDONE = B_PREADY + kPBufs, B_OEMPTY = B_PVDONE + 1,
+    // both
+    B_FINAL = B_OEMPTY + 1, B_COUNT = B_FINAL + 1
+};
+constexpr uint32_t kTmemSlotOff = kBarOff + B_COUNT * 8;
+constexpr uint32_t kAbortOff = kTmemSlotOff + 4;
+constexpr uint32_t kSmemUsed = kAbortOff + 4;
+constexpr size_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack of the dynamic base
+
+// -------------------------------------------------------------- work walk
+struct Segment {
+    int b, T, n_pages, p0, p1, split, n_split;
+};
+
+struct PartWalk {
+    int bb, bp, eb, ep, bs, b;
+    __device__ void init(const DecodeParams &p, int part) {
+        const int32_t *md = p.metadata + (size_t)part * kMdInts;
+        bb = md[0];
+        bp = md[1];
+        eb = md[2];
+        ep = md[3];
+        bs = md[4];
+        b = (bb == eb && bp == ep) ? p.batch : bb;  // an empty part walks nothing
+        if (b < 0) b = p.batch;
+    }
+    __device__ bool next(const DecodeParams &p, Segment &s) {
+        if (b >= p.batch || b > eb || (b == eb && ep == 0)) return false;
+        int T = p.seqlens[b];
+        if (T < 0) T = 0;
+        if (T > p.max_blocks * kPage) T = p.max_blocks * kPage;
+        s.b = b;
+        s.T = T;
+        s.n_pages = (T + kPage - 1) / kPage;
+        s.p1 = (b == eb) ? min(ep, s.n_pages) : s.n_pages;
+        s.p0 = (b == bb) ? min(bp, s.p1) : 0;
+        s.split = (b == bb) ? bs : 0;
+        s.n_split = p.num_splits[b + 1] - p.num_splits[b];
+        ++b;
+        return true;
+    }
+};
+
+struct Ctx {
+    uint8_t *base;
+    uint64_t *bars;
+    volatile int *abort_flag;
+    unsigned int *status;
+    uint32_t peer;  // the other CTA's rank
+    __device__ uint64_t *bar(int i) const { return bars + i; }
+};
+
+// bounded wait that also gives up when this CTA was told to abort
+template <bool kCluster = false>
+__device__ __forceinline__ bool wait(const Ctx &c, int bar_idx, uint32_t parity) {
+    const uint32_t a = smem_u32(c.bar(bar_idx));
+    if (kCluster ? mbar_test_cluster(a, parity) : mbar_test(a, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        for (int i = 0; i < 32; ++i)
+            if (kCluster ? mbar_test_cluster(a, parity) : mbar_test(a, parity)) return true;
+        if (*c.abort_flag) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(c.status, MLA_DEVERR_TIMEOUT);
+            *c.abort_flag = 1;
+            // tell the peer CTA to stop waiting on us
+            asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(mapa(smem_u32((const void *)c.abort_flag), c.peer)),
+                         "r"(1)
+                         : "memory");
+            return false;
+        }
+    }
+}
+
+// the same wait taken by every lane of a warp, with one outcome for all of
+// them (the row warps run warp-collective tcgen05.ld/st after their waits)
+template <bool kCluster = false>
+__device__ __forceinline__ bool warp_wait(const Ctx &c, int bar_idx, uint32_t parity) {
+    return __all_sync(0xffffffffu, wait<kCluster>(c, bar_idx, parity));
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ int safe_block(const DecodeParams &p, int b, int page) {
+    const int blk = p.block_table[(size_t)b * p.max_blocks + page];
+    if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+        atomicOr(p.status, MLA_DEVERR_BLOCK_ID);
+        return 0;
+    }
+    return blk;
+}
+
+// -------------------------------------------------------------- roles
+// TMA producer (one lane): streams the part's pages through the stage ring.
+__device__ void producer(const DecodeParams &p, const Ctx &c, const CUtensorMap *map, bool is_score, int part) {
+    const int stages = is_score ? kKStages : kVStages;
+    const int chunks = is_score ? kKChunks : kVChunks;
+    const uint32_t stage_bytes = is_score ? kKStageBytes : kVStageBytes;
+    const int full = is_score ? B_KFULL : B_VFULL;
+    const int empty = is_score ? B_KEMPTY : B_VEMPTY;
+    PartWalk walk;
+    walk.init(p, part);
+    Segment s;
+    uint32_t it = 0;
+    bool ok = true;
+    while (ok && walk.next(p, s)) {
+        for (int pg = s.p0; pg < s.p1; ++pg, ++it) {
+            const int st = it % stages;
+            const uint32_t use = it / stages;
+            if (!wait(c, empty + st, (use & 1) ^ 1)) {
+                ok = false;
+                break;
+            }
+            const int blk = safe_block(p, s.b, pg);
+            mbar_arrive_expect_tx(c.bar(full + st), stage_bytes);
+            uint8_t *dst = c.base + kRingOff + st * stage_bytes;
+            for (int ch = 0; ch < chunks; ++ch) tma_load_3d(dst + ch * kChunkBytes, map, c.bar(full + st), 64 * ch, 0, blk);
+        }
+    }
+    // the last loads must have landed before this CTA may exit (already true
+    // on the normal path, where the MMA consumed them)
+    for (uint32_t k = it > (uint32_t)stages ? it - stages : 0; k < it; ++k)
+        mbar_wait(c.bar(full + (int)(k % stages)), (k / stages) & 1, c.status);
+}
+
+// Score-CTA MMA issuer: S[buf] = Q K^T for every page.
+__device__ void score_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, int part) {
+    constexpr uint32_t idesc = idesc_bf16(kTileRows, kPage, false, false);
+    PartWalk walk;
+    walk.init(p, part);
+    Segment s;
+    uint32_t it = 0, seg = 0;
+    while (walk.next(p, s)) {
+        if (!wait(c, B_QFULL, seg & 1)) return;  // Q of this segment is in TMEM
+        ++seg;
+        tc_fence_after();
+        for (int pg = s.p0; pg < s.p1; ++pg, ++it) {
+            const int st = it % kKStages, sb = it % kSBufs;
+            if (!wait(c, B_KFULL + st, (it / kKStages) & 1)) return;
+            if (!wait(c, B_SEMPTY + sb, ((it / kSBufs) & 1) ^ 1)) return;
+            tc_fence_after();
+            const uint32_t ktile = smem_u32(c.base + kRingOff + st * kKStageBytes);
+            const uint32_t d = tmem + kSCol0 + sb * kPage;
+#pragma unroll
+            for (int kk = 0; kk < kDqk / 16; ++kk) {
+                const uint64_t bd = desc_sw128(ktile + (kk / 4) * kChunkBytes + (kk % 4) * 32, 16, 1024);
+                mma_ts(d, tmem + kk * 8, bd, idesc, kk > 0);
+            }
+            mma_commit(c.bar(B_KEMPTY + st));
+            mma_commit(c.bar(B_SFULL + sb));
+        }
+    }
+}
+
+// Value-CTA MMA issuer: O (+)= P V for every page.
+__device__ void value_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, int part) {
+    constexpr uint32_t idesc = idesc_bf16(kTileRows, 256, false, true);
+    PartWalk walk;
+    walk.init(p, part);
+    Segment s;
+    uint32_t it = 0, seg = 0;
+    while (walk.next(p, s)) {
+        if (!wait(c, B_OEMPTY, (seg & 1) ^ 1)) return;  // previous segment's epilogue has read O
+        ++seg;
+        for (int pg = s.p0; pg < s.p1; ++pg, ++it) {
+            const int st = it % kVStages, pb = it % kPBufs;
+            if (!wait(c, B_VFULL + st, (it / kVStages) & 1)) return;
+            if (!wait(c, B_PREADY + pb, (it / kPBufs) & 1)) return;
+            tc_fence_after();
+            const uint32_t vtile = smem_u32(c.base + kRingOff + st * kVStageBytes);
+            const uint32_t ptile = smem_u32(c.base + kPBufOff + pb * kPBytes);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int k = 0; k < kPage / 16; ++k) {
+                    const uint64_t ad = desc_sw128(ptile + k * 32, 16, 1024);
+                    const uint64_t bd = desc_sw128(vtile + h * 4 * kChunkBytes + k * 2048, kChunkBytes, 1024);
+                    mma_ss(tmem + h * 256, ad, bd, idesc, (pg > s.p0 || k > 0) ? 1u : 0u);
+                }
+            mma_commit(c.bar(B_VEMPTY + st));
+            mma_commit(c.bar(B_PVDONE));
+            mma_commit_multicast(c.bar(B_PFREE + pb), (uint16_t)(1u << c.peer));
+        }
+    }
+}
+
+// Score-CTA row warps: Q -> TMEM, masked online softmax, P and factors -> peer.
+__device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, int part, int tile) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = 32 * (warp & 3) + lane;                // tile row = TMEM lane
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const int gr = tile * kTileRows + r;                 // row within the sequence's rows
+    const bool row_ok = gr < p.rows;
+    const int qi = row_ok ? gr / p.h_q : 0;              // query token index
+    const uint32_t peer_pbuf = mapa(smem_u32(c.base + kPBufOff), c.peer);
+    const uint32_t peer_msg = mapa(smem_u32(c.base + kMsgOff), c.peer);
+    const uint32_t peer_pfull = mapa(smem_u32(c.bar(B_PFULL)), c.peer);
+    PartWalk walk;
+    walk.init(p, part);
+    Segment s;
+    uint32_t it = 0;
+    while (walk.next(p, s)) {
+        const int T_row = p.causal ? s.T - p.s_q + qi + 1 : s.T;
+        if (s.p1 > s.p0) {
+            // Q rows into TMEM columns [0, 288): bf16 pairs, row r in lane r;
+            // three 64-dim chunks (24 loads) in flight at a time
+            const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q + ((size_t)s.b * p.rows + (row_ok ? gr : 0)) * kDqk);
+#pragma unroll 1
+            for (int ch0 = 0; ch0 < kKChunks; ch0 += 3) {
+                uint4 x[24];
+#pragma unroll
+                for (int j = 0; j < 24; ++j) x[j] = row_ok ? __ldg(qrow + ch0 * 8 + j) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int k = 0; k < 3; ++k) {
+                    uint32_t v[32];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        v[4 * j] = x[8 * k + j].x;
+                        v[4 * j + 1] = x[8 * k + j].y;
+                        v[4 * j + 2] = x[8 * k + j].z;
+                        v[4 * j + 3] = x[8 * k + j].w;
+                    }
+                    tmem_st32(tmem + lane_base + (ch0 + k) * 32, v);
+                }
+            }
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(c.bar(B_QFULL));
+
+        float m = -CUDART_INF_F, l = 0.f;
+        for (int pg = s.p0; pg < s.p1; ++pg, ++it) {
+            const int sb = it % kSBufs, pb = it % kPBufs;
+            if (!warp_wait(c, B_SFULL + sb, (it / kSBufs) & 1)) return;
+            tc_fence_after();
+            uint32_t sr[64];
+            {
+                uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
+                uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
+                tmem_ld32(tmem + lane_base + kSCol0 + sb * kPage, lo);
+                tmem_ld32(tmem + lane_base + kSCol0 + sb * kPage + 32, hi);
+            }
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(c.bar(B_SEMPTY + sb));
+
+            // keys of this page visible to this row
+            int nvalid = row_ok ? T_row - pg * kPage : 0;
+            nvalid = nvalid < 0 ? 0 : (nvalid > kPage ? kPage : nvalid);
+            float x[64];
+            float mx = -CUDART_INF_F;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                x[j] = (j < nvalid) ? __uint_as_float(sr[j]) * p.scale_log2 : -CUDART_INF_F;
+                mx = fmaxf(mx, x[j]);
+            }
+            float fac = 1.f;
+            if (mx > m + kRescaleLog2 || (m == -CUDART_INF_F && mx > -CUDART_INF_F)) {
+                fac = ex2(m - mx);  // 0 when m was -inf
+                m = mx;
+            }
+            float sum = 0.f;
+            uint32_t pk[32];
+            if (m == -CUDART_INF_F) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) pk[j] = 0u;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float a = ex2(x[2 * j] - m), b = ex2(x[2 * j + 1] - m);
+                    sum += a + b;
+                    pk[j] = pack_bf16(a, b);
+                }
+            }
+            l = l * fac + sum;
+
+            // P buffer pb is free once the value CTA's MMA of page it - 2 is done
+            if (!warp_wait<true>(c, B_PFREE + pb, ((it / kPBufs) & 1) ^ 1)) return;
+            const uint32_t prow = peer_pbuf + pb * kPBytes + r * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                st_cluster_v4(prow + ((j ^ (r & 7)) * 16), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            const uint32_t msg = peer_msg + pb * kMsgBytes;
+            st_cluster_f32(msg + r * 4, fac);
+            if (pg == s.p1 - 1) st_cluster_f32(msg + (kTileRows + r) * 4, l > 0.f ? 1.f / l : 0.f);
+            fence_proxy_async();
+            mbar_arrive_remote(peer_pfull + pb * 8);
+        }
+        // LSE of this row over the segment (natural log)
+        if (row_ok) {
+            const float lse_row = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+            if (s.n_split <= 1) {
+                p.lse[(size_t)s.b * p.rows + gr] = lse_row;
+            } else {
+                const int slot = p.num_splits[s.b] + s.split;
+                if (slot >= 0 && slot < p.max_splits) p.lse_accum[(size_t)slot * p.rows + gr] = lse_row;
+                else atomicOr(p.status, MLA_DEVERR_SEQLEN);
+            }
+        }
+    }
+    // the peer's last commits arrive on our P-free barriers: let them land
+    // before this CTA can leave
+    for (uint32_t k = it > (uint32_t)kPBufs ? it - kPBufs : 0; k < it; ++k)
+        if (!warp_wait<true>(c, B_PFREE + (int)(k % kPBufs), (k / kPBufs) & 1)) return;
+}
+
+// Value-CTA row warps: V tail zeroing, lazy O rescale, epilogue.
+__device__ void value_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, int part, int tile) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = 32 * (warp & 3) + lane;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const int gr = tile * kTileRows + r;
+    const bool row_ok = gr < p.rows;
+    const int tid = threadIdx.x - 64;  // 0..127 among the row warps
+    PartWalk walk;
+    walk.init(p, part);
+    Segment s;
+    uint32_t it = 0;
+    while (walk.next(p, s)) {
+        float inv_l = 0.f;
+        for (int pg = s.p0; pg < s.p1; ++pg, ++it) {
+            const int pb = it % kPBufs, st = it % kVStages;
+            if (!warp_wait<true>(c, B_PFULL + pb, (it / kPBufs) & 1)) return;
+            const float *msg = reinterpret_cast<const float *>(c.base + kMsgOff + pb * kMsgBytes);
+            const float fac = msg[r];
+            if (pg == s.p1 - 1) inv_l = msg[kTileRows + r];
+            // rows past the sequence's end in its last page: zero them in V so
+            // that garbage (even NaN) times a zero weight stays zero
+            const int tail = s.T - pg * kPage;
+            if (tail < kPage) {
+                if (!warp_wait(c, B_VFULL + st, (it / kVStages) & 1)) return;
+                uint8_t *vt = c.base + kRingOff + st * kVStageBytes;
+                const int rows_bad = kPage - tail;
+                for (int idx = tid; idx < kVChunks * rows_bad * 8; idx += 128) {
+                    const int ch = idx / (rows_bad * 8);
+                    const int rr = tail + (idx / 8) % rows_bad;
+                    const int piece = idx % 8;
+                    *reinterpret_cast<uint4 *>(vt + ch * kChunkBytes + rr * 128 + piece * 16) = make_uint4(0, 0, 0, 0);
+                }
+            }
+            fence_proxy_async_smem();
+            // lazy rescale of this row of O before the next accumulation
+            const bool need = (pg > s.p0) && (fac != 1.f);
+            if (__any_sync(0xffffffffu, need)) {
+                if (!warp_wait(c, B_PVDONE, (it - 1) & 1)) return;  // every earlier P V has landed
+                tc_fence_after();
+#pragma unroll 1
+                for (int ch = 0; ch < 16; ++ch) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_base + ch * 32, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * fac);
+                    tmem_st32(tmem + lane_base + ch * 32, v);
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            mbar_arrive(c.bar(B_PREADY + pb));
+        }
+        // epilogue: O / l -> bf16 output, or fp32 partial for the combine
+        if (s.p1 > s.p0) {
+            if (!warp_wait(c, B_PVDONE, (it - 1) & 1)) return;
+            tc_fence_after();
+        }
+        const bool split = s.n_split > 1;
+        int slot = 0;
+        if (split) {
+            slot = p.num_splits[s.b] + s.split;
+            if (slot < 0 || slot >= p.max_splits) {
+                atomicOr(p.status, MLA_DEVERR_SEQLEN);
+                slot = -1;
+            }
+        }
+        const size_t out_row = split ? (size_t)slot * p.rows + gr : (size_t)s.b * p.rows + gr;
+#pragma unroll 1
+        for (int ch = 0; ch < 16; ++ch) {
+            uint32_t v[32];
+            if (s.p1 > s.p0) {
+                tmem_ld32(tmem + lane_base + ch * 32, v);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0u;
+            }
+            if (!row_ok || slot < 0) continue;
+            if (split) {
+                float4 *dst = reinterpret_cast<float4 *>(p.o_accum + out_row * kDv + ch * 32);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    dst[j] = make_float4(__uint_as_float(v[4 * j]) * inv_l, __uint_as_float(v[4 * j + 1]) * inv_l,
+                                         __uint_as_float(v[4 * j + 2]) * inv_l, __uint_as_float(v[4 * j + 3]) * inv_l);
+            } else {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.o + out_row * kDv + ch * 32);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint4 w;
+                    w.x = pack_bf16(__uint_as_float(v[8 * j]) * inv_l, __uint_as_float(v[8 * j + 1]) * inv_l);
+                    w.y = pack_bf16(__uint_as_float(v[8 * j + 2]) * inv_l, __uint_as_float(v[8 * j + 3]) * inv_l);
+                    w.z = pack_bf16(__uint_as_float(v[8 * j + 4]) * inv_l, __uint_as_float(v[8 * j + 5]) * inv_l);
+                    w.w = pack_bf16(__uint_as_float(v[8 * j + 6]) * inv_l, __uint_as_float(v[8 * j + 7]) * inv_l);
+                    dst[j] = w;
+                }
+            }
+        }
+        tc_fence_before();
+        mbar_arrive(c.bar(B_OEMPTY));
+    }
+}
+
+// -------------------------------------------------------------- kernel
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t rank = cluster_ctarank();
+    const bool is_score = rank == 0;
+    const int part = blockIdx.x >> 1;
+    const int tile = blockIdx.y;
+    const int warp = threadIdx.x >> 5;
+
+    Ctx c;
+    c.base = base;
+    c.bars = reinterpret_cast<uint64_t *>(base + kBarOff);
+    c.abort_flag = reinterpret_cast<volatile int *>(base + kAbortOff);
+    c.status = p.status;
+    c.peer = rank ^ 1u;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + kTmemSlotOff);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kKStages; ++i) {
+            mbar_init(c.bar(B_KFULL + i), 1);
+            mbar_init(c.bar(B_KEMPTY + i), 1);
+        }
+        for (int i = 0; i < kSBufs; ++i) {
+            mbar_init(c.bar(B_SFULL + i), 1);
+            mbar_init(c.bar(B_SEMPTY + i), 128);
+        }
+        mbar_init(c.bar(B_QFULL), 128);
+        for (int i = 0; i < kPBufs; ++i) {
+            mbar_init(c.bar(B_PFREE + i), 1);
+            mbar_init(c.bar(B_PFULL + i), 128);
+            mbar_init(c.bar(B_PREADY + i), 128);
+        }
+        for (int i = 0; i < kVStages; ++i) {
+            mbar_init(c.bar(B_VFULL + i), 1);
+            mbar_init(c.bar(B_VEMPTY + i), 1);
+        }
+        mbar_init(c.bar(B_PVDONE), 1);
+        mbar_init(c.bar(B_OEMPTY), 128);
+        mbar_init(c.bar(B_FINAL), 1);
+        *c.abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&kv_map);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_arrive();
+    cluster_wait();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (elect_one_lane()) producer(p, c, &kv_map, is_score, part);
+    } else if (warp == 1) {
+        if (elect_one_lane()) {
+            if (is_score) score_mma(p, c, tmem, part);
+            else value_mma(p, c, tmem, part);
+            // all MMAs this thread issued must finish before TMEM is released
+            mma_commit(c.bar(B_FINAL));
+            mbar_wait(c.bar(B_FINAL), 0, c.status);
+        }
+        __syncwarp();
+    } else {
+        if (is_score) score_rows(p, c, tmem, part, tile);
+        else value_rows(p, c, tmem, part, tile);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    // neither CTA may leave while its peer can still touch its shared memory
+    cluster_arrive();
+    cluster_wait();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// -------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// kcache [num_blocks][64][576] bf16 viewed as a 3-D tensor {576, 64, num_blocks};
+// one box is a 64-dim x 64-token chunk, stored with the 128-byte swizzle that
+// the tcgen05 K-major (K) and MN-major (V) operand descriptors expect.
+bool make_kv_map(CUtensorMap *m, const void *kcache, int64_t num_blocks) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)kDqk, (cuuint64_t)kPage, (cuuint64_t)num_blocks};
+    cuuint64_t strides[2] = {(cuuint64_t)kDqk * 2, (cuuint64_t)kPage * kDqk * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)kPage, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(kcache), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int kMaxDevices = 64;
+bool g_attr_set[kMaxDevices] = {};
+std::mutex g_attr_mutex;
+
+cudaError_t prepare(int dev) {
+    std::lock_guard<std::mutex> lock(g_attr_mutex);
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (g_attr_set[dev]) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(split_kv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e == cudaSuccess) g_attr_set[dev] = true;
+    return e;
+}
+
+}  // namespace
+
+int split_kv_tc_tile_rows() { return kTileRows; }
+
+cudaError_t split_kv_tc_max_pairs(int *pairs) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if ((e = prepare(dev)) != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    cfg.numAttrs = 0;  // the cluster shape is fixed by the kernel's attribute
+    e = cudaOccupancyMaxActiveClusters(&n, split_kv_tc_kernel, &cfg);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        cfg.numAttrs = 1;
+        e = cudaOccupancyMaxActiveClusters(&n, split_kv_tc_kernel, &cfg);
+    }
+    if (e != cudaSuccess) return e;
+    *pairs = n;
+    return cudaSuccess;
+}
+
+cudaError_t launch_split_kv_tc(const DecodeParams &p, cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if ((e = prepare(dev)) != cudaSuccess) return e;
+    CUtensorMap map;
+    if (!make_kv_map(&map, p.kcache, p.num_blocks)) return cudaErrorInvalidValue;
+    const int tiles = (p.rows + kTileRows - 1) / kTileRows;
+    dim3 grid(2 * p.num_parts, tiles, 1);
+    split_kv_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map, p);
+    return cudaGetLastError();
+}
+
+}  // namespace mla
