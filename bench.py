@@ -187,12 +187,25 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """Slowest rank's time: the all-reduce runs on the process group's own device (NCCL: GPU, gloo: CPU)."""
     if world <= 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_case(case, rank):
+    """Weak scaling: every rank decodes its own full batch of the workload, drawn with its own seed."""
+    import dataclasses
+    return case if rank == 0 else dataclasses.replace(case, seed=case.seed + 7919 * rank)
+
+
+def aggregate_gbs(bytes_per_rank, world, ms_step_slowest):
+    """Whole-job KV-cache GB/s: every rank's bytes over the slowest rank's step time."""
+    return bytes_per_rank * world / (ms_step_slowest * 1e-3) / 1e9
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -247,6 +260,7 @@ def main():
     torch.cuda.set_device(dev)
     import mla_decode_attention_latent_gb300 as mla
     mla._lib.load()
+    case = rank_case(case, rank)
 
     x = W.make_inputs(case, device=str(dev))
     sl_list = x.cache_seqlens.cpu().tolist()
@@ -297,8 +311,7 @@ def main():
     ms_total = max_over_ranks(ms_total, world)
     ms_step = ms_total / args.steps
     split_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_split)
-    total_bytes = fig["bytes"] * world
-    value = total_bytes / (ms_step * 1e-3) / 1e9
+    value = aggregate_gbs(fig["bytes"], world, ms_step)
     tflops = fig["flops"] * world / (ms_step * 1e-3) / 1e12
     pk = peaks()
     bound = "hbm"
