@@ -169,6 +169,38 @@ MLA_API int mla_decode_kvcache(const void *q, const void *kcache, int64_t num_bl
                        size_t workspace_bytes, struct CUstream_st *stream);
 
 /*
+ * mla_decode_kvcache_noalloc — mla_decode_kvcache for callers that cannot
+ * allocate device memory.
+ *
+ * The pages have no counterpart of this call; it exists for callers that may
+ * not allocate at decode time: runtimes that plan every byte of device memory
+ * up front in their own arena, plugin interfaces that pass a call its inputs
+ * and outputs but no workspace, and hot loops that must avoid an
+ * allocation's implicit synchronisation.  The arguments and results are those
+ * of mla_decode_kvcache without `workspace` / `workspace_bytes`: the split-KV
+ * scratch comes from one fixed device array of MLA_NOALLOC_SCRATCH_BYTES
+ * inside the library, which every GPU that loads the library keeps until the
+ * process exits.  No call allocates (no cudaMalloc, cudaFree or allocating
+ * library routine).
+ *  - The first call on a device looks up the array's device address with that
+ *    device current (a one-time set-up per device); make that first call
+ *    before any stream capture.
+ *  - Every call shares the array and it keeps the previous call's contents;
+ *    nothing in it needs to start at zero.  Calls whose kernels overlap on the
+ *    GPU (e.g. on two streams) race on it: order them on one stream.
+ * Errors: those of mla_decode_kvcache, and MLA_ERR_WORKSPACE when
+ * mla_workspace_bytes() for the shape exceeds MLA_NOALLOC_SCRATCH_BYTES
+ * (nothing is launched then).
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+MLA_API int mla_decode_kvcache_noalloc(const void *q, const void *kcache, int64_t num_blocks,
+                                       const int32_t *block_table, int max_blocks_per_seq,
+                                       const int32_t *cache_seqlens, int batch, int s_q, int h_q, int h_kv,
+                                       int d, int dv, const int32_t *tile_scheduler_metadata,
+                                       const int32_t *num_splits, int num_parts, float softmax_scale,
+                                       int causal, void *o, float *lse, struct CUstream_st *stream);
+
+/*
  * mla_device_status — read the device status word of the current device.
  *
  * Synchronizes the device, stores the OR of the MLA_DEVERR_* bits raised by

@@ -25,6 +25,8 @@ MLA_HEAD_DIM = 576
 MLA_V_DIM = 512
 MLA_METADATA_INTS = 8
 
+MLA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
+
 MLA_DEVERR_TIMEOUT = 0x1
 MLA_DEVERR_BLOCK_ID = 0x2
 MLA_DEVERR_SEQLEN = 0x4
@@ -37,6 +39,8 @@ SIGNATURES = {
     "mla_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "mla_decode_kvcache": (_I, [_P, _P, _I64, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _F, _I, _P, _P,
                                 _P, _SZ, _P]),
+    "mla_decode_kvcache_noalloc": (_I, [_P, _P, _I64, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _F, _I, _P,
+                                        _P, _P]),
     "mla_device_status": (_I, [ctypes.POINTER(ctypes.c_int), _I]),
     "mla_set_timing_events": (_I, [_P, _P]),
     "mla_status_string": (ctypes.c_char_p, [_I]),

@@ -119,6 +119,37 @@ def mla_decode_kvcache(q: torch.Tensor, kcache: torch.Tensor, block_table: torch
     return out, lse
 
 
+def mla_decode_kvcache_noalloc(q: torch.Tensor, kcache: torch.Tensor, block_table: torch.Tensor,
+                               cache_seqlens: torch.Tensor, dv: int, tile_scheduler_metadata: torch.Tensor,
+                               num_splits: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
+                               softmax_scale: Optional[float] = None, causal: bool = False) -> None:
+    """Decode into caller-provided ``out`` / ``lse`` without any device allocation.
+
+    For callers that cannot allocate at decode time: the split-KV scratch is
+    the library's fixed internal array (``MLA_NOALLOC_SCRATCH_BYTES``), shared
+    by every call, so calls must not overlap on the GPU.  Make the first call
+    on a device before any stream capture (it looks up the array's address).
+    """
+    for name, t, dt in (("q", q, torch.bfloat16), ("kcache", kcache, torch.bfloat16),
+                        ("block_table", block_table, torch.int32), ("cache_seqlens", cache_seqlens, torch.int32),
+                        ("tile_scheduler_metadata", tile_scheduler_metadata, torch.int32),
+                        ("num_splits", num_splits, torch.int32), ("out", out, torch.bfloat16),
+                        ("lse", lse, torch.float32)):
+        _need_cuda(name, t, dt)
+    b, s_q, h_q, d = q.shape
+    num_blocks, _, h_kv, _ = kcache.shape
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    dev = q.device
+    with torch.cuda.device(dev):
+        st = load().mla_decode_kvcache_noalloc(
+            q.data_ptr(), kcache.data_ptr(), num_blocks, block_table.data_ptr(), block_table.shape[1],
+            cache_seqlens.data_ptr(), b, s_q, h_q, h_kv, d, dv, tile_scheduler_metadata.data_ptr(),
+            num_splits.data_ptr(), tile_scheduler_metadata.shape[0], float(softmax_scale), int(bool(causal)),
+            out.data_ptr(), lse.data_ptr(), _stream_handle(dev))
+    check("mla_decode_kvcache_noalloc", st)
+
+
 def mla_device_status(clear: bool = True) -> int:
     """Synchronize and return the OR of the MLA_DEVERR_* bits kernels raised."""
     v = ctypes.c_int(0)
