@@ -23,12 +23,15 @@
 //   tcgen05 S = Q K^T  (ts, N = 64)        tcgen05 O += P V  (ss, N = 2 x 256)
 //   4 warps: mask + online softmax,        4 warps: zero the invalid tail rows
 //     P (bf16) and the per-row O              of V, rescale O rows when the
-//     rescale factor -> peer's smem           running max moved, epilogue
+//     rescale factor -> local staging         running max moved, epilogue
+//     -> one bulk copy into the peer          staged through smem
 //
 // Both CTAs read each page from global memory (the second read normally hits
-// L2).  P travels through distributed shared memory (16 KB per page); the
-// value CTA's MMA commit releases the P buffer back to the score CTA through
-// a multicast commit.  The running max is rescaled lazily: O is only
+// L2).  P and the row factors (17 KB per page) are written to local shared
+// memory and pushed into the value CTA by one asynchronous bulk copy that
+// completes on the value CTA's barrier, so the softmax warps never wait on
+// cluster round trips; the value CTA's MMA commit hands the buffer back
+// through a multicast commit.  The running max is rescaled lazily: O is only
 // corrected when a page's maximum exceeds the current one by more than 2^8.
 //
 // Warp roles (192 threads): warp 0 issues TMA, warp 1 allocates TMEM and
@@ -54,30 +57,39 @@ using namespace sm103;
 
 constexpr int kThreads = 192;
 constexpr int kTileRows = 128;                 // query rows per tile = TMEM lanes
-constexpr int kKStages = 3;                    // K ring (score CTA)
+constexpr int kKStages = 2;                    // K ring (score CTA)
 constexpr int kVStages = 2;                    // V ring (value CTA)
 constexpr int kSBufs = 3;                      // S buffers in TMEM (score CTA)
-constexpr int kPBufs = 2;                      // P buffers in the value CTA's smem
+constexpr int kPBufs = 2;                      // P buffers (staging in the score CTA, landing in the value CTA)
 constexpr int kKChunks = kDqk / 64;            // 9 chunks of 64 dims (128 B rows)
 constexpr int kVChunks = kDv / 64;             // 8
 constexpr uint32_t kChunkBytes = kPage * 128;  // 64 tokens x 128 B = 8 KB
 constexpr uint32_t kKStageBytes = kKChunks * kChunkBytes;  // 72 KB
 constexpr uint32_t kVStageBytes = kVChunks * kChunkBytes;  // 64 KB
-constexpr uint32_t kPBytes = kTileRows * 128;             // 16 KB: 128 rows x 64 bf16
+constexpr uint32_t kPBytes = kTileRows * 128;             // 16 KB: 128 rows x 64 bf16, 128B-swizzled
+constexpr uint32_t kFacOff = kPBytes;                      // then fac[128] (fp32)
+constexpr uint32_t kInvLOff = kPBytes + kTileRows * 4;     // then inv_l[128] (fp32)
+constexpr uint32_t kPMsgBytes = kPBytes + 2 * kTileRows * 4;  // 17 KB, a multiple of 1 KB
 constexpr uint32_t kQCols = kDqk / 2;                      // Q: 288 TMEM columns of bf16 pairs
 constexpr uint32_t kSCol0 = kQCols;                        // S buffers follow Q
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (log2 units)
+constexpr uint32_t kEpiCols = 64;                          // epilogue chunk: 64 fp32 columns
+constexpr uint32_t kEpiStride = kEpiCols * 4 + 16;         // padded row stride (conflict-free v4 stores)
 
-// shared-memory layout (offsets from the 1024-byte aligned base); both CTAs
-// use the same offsets so that peer addresses are plain mapa() translations
-constexpr uint32_t kRingOff = 0;
-constexpr uint32_t kRingBytes = kKStages * kKStageBytes;                 // 216 KB
-constexpr uint32_t kPBufOff = kVStages * kVStageBytes;                   // value CTA: after its V ring
-constexpr uint32_t kMsgOff = kPBufOff + kPBufs * kPBytes;                // value CTA: per-page row data
-constexpr uint32_t kMsgBytes = 2 * kTileRows * sizeof(float);            // fac[128], inv_l[128]
-static_assert(kMsgOff + kPBufs * kMsgBytes <= kRingBytes, "value CTA buffers must fit the ring region");
-constexpr uint32_t kBarOff = kRingBytes;
+// shared-memory layout (offsets from the 1024-byte aligned base)
+// score CTA: [K ring 2 x 72 KB][P staging 2 x 17 KB]
+constexpr uint32_t kKRingOff = 0;
+constexpr uint32_t kStageOff = kKRingOff + kKStages * kKStageBytes;
+constexpr uint32_t kScoreEnd = kStageOff + kPBufs * kPMsgBytes;
+// value CTA: [V ring 2 x 64 KB][P landing 2 x 17 KB][epilogue staging 34 KB]
+constexpr uint32_t kVRingOff = 0;
+constexpr uint32_t kPBufOff = kVRingOff + kVStages * kVStageBytes;
+constexpr uint32_t kEpiOff = kPBufOff + kPBufs * kPMsgBytes;
+constexpr uint32_t kValueEnd = kEpiOff + kTileRows * kEpiStride;
+// barriers at the same offset in both CTAs (the peer arrives on them)
+constexpr uint32_t kBarOff = ((kScoreEnd > kValueEnd ? kScoreEnd : kValueEnd) + 1023u) & ~1023u;
+static_assert(kStageOff % 1024 == 0 && kPBufOff % 1024 == 0 && kPMsgBytes % 1024 == 0, "swizzled tiles need 1 KB alignment");
 
 enum Bar {
     // score CTA
@@ -86,13 +98,16 @@ enum Bar {
     // value CTA
     B_VFULL = B_PFREE + kPBufs, B_VEMPTY = B_VFULL + kVStages, B_PFULL = B_VEMPTY + kVStages,
     B_PREADY = B_PFULL + kPBufs, B_PVDONE = B_PREADY + kPBufs, B_OEMPTY = B_PVDONE + 1,
+    B_EPI = B_OEMPTY + 1,                   // group sync of the value row warps (epilogue)
+    B_SREADY = B_EPI + 1,                   // score CTA: staging pb written by all row threads
     // both
-    B_FINAL = B_OEMPTY + 1, B_COUNT = B_FINAL + 1
+    B_FINAL = B_SREADY + kPBufs, B_COUNT = B_FINAL + 1
 };
 constexpr uint32_t kTmemSlotOff = kBarOff + B_COUNT * 8;
 constexpr uint32_t kAbortOff = kTmemSlotOff + 4;
 constexpr uint32_t kSmemUsed = kAbortOff + 4;
 constexpr size_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack of the dynamic base
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 // -------------------------------------------------------------- work walk
 struct Segment {
@@ -166,6 +181,16 @@ __device__ __forceinline__ bool warp_wait(const Ctx &c, int bar_idx, uint32_t pa
     return __all_sync(0xffffffffu, wait<kCluster>(c, bar_idx, parity));
 }
 
+// barrier among the 128 row threads built on an mbarrier, so that it is
+// bounded like every other wait (a plain bar.sync would hang if a peer warp
+// had given up on a timeout)
+__device__ __forceinline__ bool group_sync(const Ctx &c, int bar_idx, uint32_t &phase) {
+    mbar_arrive(c.bar(bar_idx));
+    const bool ok = warp_wait(c, bar_idx, phase & 1);
+    ++phase;
+    return ok;
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -183,15 +208,25 @@ __device__ __forceinline__ int safe_block(const DecodeParams &p, int b, int page
 
 // -------------------------------------------------------------- roles
 // TMA producer (one lane): streams the part's pages through the stage ring.
-__device__ void producer(const DecodeParams &p, const Ctx &c, const CUtensorMap *map, bool is_score, int part) {
+// The score CTA's producer first asks L2 for the Q rows of every segment of
+// the part, so that the row warps' Q loads at segment starts hit L2.
+__device__ void producer(const DecodeParams &p, const Ctx &c, const CUtensorMap *map, bool is_score, int part,
+                         int tile) {
     const int stages = is_score ? kKStages : kVStages;
     const int chunks = is_score ? kKChunks : kVChunks;
     const uint32_t stage_bytes = is_score ? kKStageBytes : kVStageBytes;
     const int full = is_score ? B_KFULL : B_VFULL;
     const int empty = is_score ? B_KEMPTY : B_VEMPTY;
     PartWalk walk;
-    walk.init(p, part);
     Segment s;
+    if (is_score) {
+        const int rows = min(kTileRows, p.rows - tile * kTileRows);
+        walk.init(p, part);
+        while (walk.next(p, s))
+            if (s.p1 > s.p0 && rows > 0)
+                prefetch_l2(p.q + ((size_t)s.b * p.rows + (size_t)tile * kTileRows) * kDqk, (uint32_t)rows * kDqk * 2);
+    }
+    walk.init(p, part);
     uint32_t it = 0;
     bool ok = true;
     while (ok && walk.next(p, s)) {
@@ -204,7 +239,7 @@ __device__ void producer(const DecodeParams &p, const Ctx &c, const CUtensorMap 
             }
             const int blk = safe_block(p, s.b, pg);
             mbar_arrive_expect_tx(c.bar(full + st), stage_bytes);
-            uint8_t *dst = c.base + kRingOff + st * stage_bytes;
+            uint8_t *dst = c.base + st * stage_bytes;  // both rings start at offset 0
             for (int ch = 0; ch < chunks; ++ch) tma_load_3d(dst + ch * kChunkBytes, map, c.bar(full + st), 64 * ch, 0, blk);
         }
     }
@@ -230,7 +265,7 @@ __device__ void score_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, in
             if (!wait(c, B_KFULL + st, (it / kKStages) & 1)) return;
             if (!wait(c, B_SEMPTY + sb, ((it / kSBufs) & 1) ^ 1)) return;
             tc_fence_after();
-            const uint32_t ktile = smem_u32(c.base + kRingOff + st * kKStageBytes);
+            const uint32_t ktile = smem_u32(c.base + kKRingOff + st * kKStageBytes);
             const uint32_t d = tmem + kSCol0 + sb * kPage;
 #pragma unroll
             for (int kk = 0; kk < kDqk / 16; ++kk) {
@@ -258,8 +293,8 @@ __device__ void value_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, in
             if (!wait(c, B_VFULL + st, (it / kVStages) & 1)) return;
             if (!wait(c, B_PREADY + pb, (it / kPBufs) & 1)) return;
             tc_fence_after();
-            const uint32_t vtile = smem_u32(c.base + kRingOff + st * kVStageBytes);
-            const uint32_t ptile = smem_u32(c.base + kPBufOff + pb * kPBytes);
+            const uint32_t vtile = smem_u32(c.base + kVRingOff + st * kVStageBytes);
+            const uint32_t ptile = smem_u32(c.base + kPBufOff + pb * kPMsgBytes);
 #pragma unroll
             for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -283,8 +318,8 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
     const int gr = tile * kTileRows + r;                 // row within the sequence's rows
     const bool row_ok = gr < p.rows;
     const int qi = row_ok ? gr / p.h_q : 0;              // query token index
-    const uint32_t peer_pbuf = mapa(smem_u32(c.base + kPBufOff), c.peer);
-    const uint32_t peer_msg = mapa(smem_u32(c.base + kMsgOff), c.peer);
+    const bool issuer = threadIdx.x == 64;               // pushes each page to the peer
+    const uint32_t peer_buf = mapa(smem_u32(c.base + kPBufOff), c.peer);
     const uint32_t peer_pfull = mapa(smem_u32(c.bar(B_PFULL)), c.peer);
     PartWalk walk;
     walk.init(p, part);
@@ -365,17 +400,23 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
             }
             l = l * fac + sum;
 
-            // P buffer pb is free once the value CTA's MMA of page it - 2 is done
+            // staging pb is free once the value CTA's MMA of page it - 2 is
+            // done: that MMA consumed the bulk copy made from it
             if (!warp_wait<true>(c, B_PFREE + pb, ((it / kPBufs) & 1) ^ 1)) return;
-            const uint32_t prow = peer_pbuf + pb * kPBytes + r * 128;
+            uint8_t *stage = c.base + kStageOff + pb * kPMsgBytes;
+            uint4 *prow = reinterpret_cast<uint4 *>(stage + r * 128);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                st_cluster_v4(prow + ((j ^ (r & 7)) * 16), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-            const uint32_t msg = peer_msg + pb * kMsgBytes;
-            st_cluster_f32(msg + r * 4, fac);
-            if (pg == s.p1 - 1) st_cluster_f32(msg + (kTileRows + r) * 4, l > 0.f ? 1.f / l : 0.f);
-            fence_proxy_async();
-            mbar_arrive_remote(peer_pfull + pb * 8);
+            for (int j = 0; j < 8; ++j) prow[j ^ (r & 7)] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            reinterpret_cast<float *>(stage + kFacOff)[r] = fac;
+            if (pg == s.p1 - 1) reinterpret_cast<float *>(stage + kInvLOff)[r] = l > 0.f ? 1.f / l : 0.f;
+            fence_proxy_async_smem();
+            mbar_arrive(c.bar(B_SREADY + pb));
+            if (issuer) {
+                if (!wait(c, B_SREADY + pb, (it / kPBufs) & 1)) return;
+                const uint32_t bar = peer_pfull + pb * 8;
+                mbar_arrive_expect_tx_remote(bar, kPMsgBytes);
+                bulk_copy_to_peer(peer_buf + pb * kPMsgBytes, stage, kPMsgBytes, bar);
+            }
         }
         // LSE of this row over the segment (natural log)
         if (row_ok) {
@@ -390,7 +431,7 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
         }
     }
     // the peer's last commits arrive on our P-free barriers: let them land
-    // before this CTA can leave
+    // before this CTA can leave (this also covers the last bulk copies)
     for (uint32_t k = it > (uint32_t)kPBufs ? it - kPBufs : 0; k < it; ++k)
         if (!warp_wait<true>(c, B_PFREE + (int)(k % kPBufs), (k / kPBufs) & 1)) return;
 }
@@ -400,9 +441,9 @@ __device__ void value_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = 32 * (warp & 3) + lane;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    const int gr = tile * kTileRows + r;
-    const bool row_ok = gr < p.rows;
     const int tid = threadIdx.x - 64;  // 0..127 among the row warps
+    uint8_t *epi = c.base + kEpiOff;
+    uint32_t epi_phase = 0;
     PartWalk walk;
     walk.init(p, part);
     Segment s;
@@ -412,15 +453,15 @@ __device__ void value_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
         for (int pg = s.p0; pg < s.p1; ++pg, ++it) {
             const int pb = it % kPBufs, st = it % kVStages;
             if (!warp_wait<true>(c, B_PFULL + pb, (it / kPBufs) & 1)) return;
-            const float *msg = reinterpret_cast<const float *>(c.base + kMsgOff + pb * kMsgBytes);
-            const float fac = msg[r];
-            if (pg == s.p1 - 1) inv_l = msg[kTileRows + r];
+            const uint8_t *buf = c.base + kPBufOff + pb * kPMsgBytes;
+            const float fac = reinterpret_cast<const float *>(buf + kFacOff)[r];
+            if (pg == s.p1 - 1) inv_l = reinterpret_cast<const float *>(buf + kInvLOff)[r];
             // rows past the sequence's end in its last page: zero them in V so
             // that garbage (even NaN) times a zero weight stays zero
             const int tail = s.T - pg * kPage;
             if (tail < kPage) {
                 if (!warp_wait(c, B_VFULL + st, (it / kVStages) & 1)) return;
-                uint8_t *vt = c.base + kRingOff + st * kVStageBytes;
+                uint8_t *vt = c.base + kVRingOff + st * kVStageBytes;
                 const int rows_bad = kPage - tail;
                 for (int idx = tid; idx < kVChunks * rows_bad * 8; idx += 128) {
                     const int ch = idx / (rows_bad * 8);
@@ -428,8 +469,8 @@ __device__ void value_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
                     const int piece = idx % 8;
                     *reinterpret_cast<uint4 *>(vt + ch * kChunkBytes + rr * 128 + piece * 16) = make_uint4(0, 0, 0, 0);
                 }
+                fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
             // lazy rescale of this row of O before the next accumulation
             const bool need = (pg > s.p0) && (fac != 1.f);
             if (__any_sync(0xffffffffu, need)) {
@@ -449,8 +490,11 @@ __device__ void value_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
             tc_fence_before();
             mbar_arrive(c.bar(B_PREADY + pb));
         }
-        // epilogue: O / l -> bf16 output, or fp32 partial for the combine
-        if (s.p1 > s.p0) {
+        // epilogue: O / l -> bf16 output, or fp32 partial for the combine.
+        // Each 64-column chunk goes TMEM -> registers -> smem (row per
+        // thread), then every warp writes 32 whole rows with coalesced stores.
+        const bool has_pages = s.p1 > s.p0;
+        if (has_pages) {
             if (!warp_wait(c, B_PVDONE, (it - 1) & 1)) return;
             tc_fence_after();
         }
@@ -459,40 +503,60 @@ __device__ void value_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
         if (split) {
             slot = p.num_splits[s.b] + s.split;
             if (slot < 0 || slot >= p.max_splits) {
-                atomicOr(p.status, MLA_DEVERR_SEQLEN);
+                if (tid == 0) atomicOr(p.status, MLA_DEVERR_SEQLEN);
                 slot = -1;
             }
         }
-        const size_t out_row = split ? (size_t)slot * p.rows + gr : (size_t)s.b * p.rows + gr;
+        const int wrow0 = 32 * (tid >> 5);  // rows this warp writes out
 #pragma unroll 1
-        for (int ch = 0; ch < 16; ++ch) {
-            uint32_t v[32];
-            if (s.p1 > s.p0) {
-                tmem_ld32(tmem + lane_base + ch * 32, v);
+        for (int ch = 0; ch < kDv / (int)kEpiCols; ++ch) {
+            uint32_t v[64];
+            if (has_pages) {
+                uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+                uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
+                tmem_ld32(tmem + lane_base + ch * kEpiCols, lo);
+                tmem_ld32(tmem + lane_base + ch * kEpiCols + 32, hi);
                 tmem_wait_ld();
             } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = 0u;
+                for (int j = 0; j < 64; ++j) v[j] = 0u;
             }
-            if (!row_ok || slot < 0) continue;
-            if (split) {
-                float4 *dst = reinterpret_cast<float4 *>(p.o_accum + out_row * kDv + ch * 32);
+            float4 *srow = reinterpret_cast<float4 *>(epi + r * kEpiStride);
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    dst[j] = make_float4(__uint_as_float(v[4 * j]) * inv_l, __uint_as_float(v[4 * j + 1]) * inv_l,
-                                         __uint_as_float(v[4 * j + 2]) * inv_l, __uint_as_float(v[4 * j + 3]) * inv_l);
-            } else {
-                uint4 *dst = reinterpret_cast<uint4 *>(p.o + out_row * kDv + ch * 32);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint4 w;
-                    w.x = pack_bf16(__uint_as_float(v[8 * j]) * inv_l, __uint_as_float(v[8 * j + 1]) * inv_l);
-                    w.y = pack_bf16(__uint_as_float(v[8 * j + 2]) * inv_l, __uint_as_float(v[8 * j + 3]) * inv_l);
-                    w.z = pack_bf16(__uint_as_float(v[8 * j + 4]) * inv_l, __uint_as_float(v[8 * j + 5]) * inv_l);
-                    w.w = pack_bf16(__uint_as_float(v[8 * j + 6]) * inv_l, __uint_as_float(v[8 * j + 7]) * inv_l);
-                    dst[j] = w;
+            for (int j = 0; j < 16; ++j)
+                srow[j] = make_float4(__uint_as_float(v[4 * j]) * inv_l, __uint_as_float(v[4 * j + 1]) * inv_l,
+                                      __uint_as_float(v[4 * j + 2]) * inv_l, __uint_as_float(v[4 * j + 3]) * inv_l);
+            if (!group_sync(c, B_EPI, epi_phase)) return;
+            if (slot >= 0) {
+                if (split) {
+                    // fp32: 256 B per row chunk, two rows per warp store
+#pragma unroll 4
+                    for (int k = 0; k < 16; ++k) {
+                        const int row = wrow0 + 2 * k + (lane >> 4);
+                        const int g = tile * kTileRows + row;
+                        const float4 val = reinterpret_cast<const float4 *>(epi + row * kEpiStride)[lane & 15];
+                        if (g < p.rows)
+                            reinterpret_cast<float4 *>(p.o_accum + ((size_t)slot * p.rows + g) * kDv + ch * kEpiCols)[lane & 15] = val;
+                    }
+                } else {
+                    // bf16: 128 B per row chunk, four rows per warp store
+#pragma unroll 4
+                    for (int k = 0; k < 8; ++k) {
+                        const int row = wrow0 + 4 * k + (lane >> 3);
+                        const int g = tile * kTileRows + row;
+                        const float4 *src = reinterpret_cast<const float4 *>(epi + row * kEpiStride) + 2 * (lane & 7);
+                        const float4 a = src[0], b = src[1];
+                        uint4 w;
+                        w.x = pack_bf16(a.x, a.y);
+                        w.y = pack_bf16(a.z, a.w);
+                        w.z = pack_bf16(b.x, b.y);
+                        w.w = pack_bf16(b.z, b.w);
+                        if (g < p.rows)
+                            reinterpret_cast<uint4 *>(p.o + ((size_t)s.b * p.rows + g) * kDv + ch * kEpiCols)[lane & 7] = w;
+                    }
                 }
             }
+            if (!group_sync(c, B_EPI, epi_phase)) return;
         }
         tc_fence_before();
         mbar_arrive(c.bar(B_OEMPTY));
@@ -530,7 +594,7 @@ split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParam
         mbar_init(c.bar(B_QFULL), 128);
         for (int i = 0; i < kPBufs; ++i) {
             mbar_init(c.bar(B_PFREE + i), 1);
-            mbar_init(c.bar(B_PFULL + i), 128);
+            mbar_init(c.bar(B_PFULL + i), 1);
             mbar_init(c.bar(B_PREADY + i), 128);
         }
         for (int i = 0; i < kVStages; ++i) {
@@ -539,6 +603,8 @@ split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParam
         }
         mbar_init(c.bar(B_PVDONE), 1);
         mbar_init(c.bar(B_OEMPTY), 128);
+        mbar_init(c.bar(B_EPI), 128);
+        for (int i = 0; i < kPBufs; ++i) mbar_init(c.bar(B_SREADY + i), 128);
         mbar_init(c.bar(B_FINAL), 1);
         *c.abort_flag = 0;
         fence_mbar_init();
@@ -556,7 +622,7 @@ split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParam
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        if (elect_one_lane()) producer(p, c, &kv_map, is_score, part);
+        if (elect_one_lane()) producer(p, c, &kv_map, is_score, part, tile);
     } else if (warp == 1) {
         if (elect_one_lane()) {
             if (is_score) score_mma(p, c, tmem, part);
