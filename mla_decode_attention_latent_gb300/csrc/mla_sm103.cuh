@@ -115,9 +115,13 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// arrive on a peer CTA's barrier and raise its expected transaction bytes
-__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t cluster_addr, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_addr),
+// arrive on a peer CTA's barrier and raise its expected transaction bytes.
+// Relaxed: it orders none of this thread's earlier writes (a release at
+// cluster scope would wait for them to become visible cluster-wide); use it
+// when the data the phase guards arrives by a transaction that completes on
+// the same barrier.
+__device__ __forceinline__ void mbar_arrive_expect_tx_remote_relaxed(uint32_t cluster_addr, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_addr),
                  "r"(bytes)
                  : "memory");
 }
@@ -139,6 +143,17 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
         "[%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+// 3-D tiled load written to the same shared-memory offset of every CTA in
+// `cta_mask`; completes tx bytes on the barrier at `bar`'s offset in each.
+__device__ __forceinline__ void tma_load_3d_multicast(void *dst, const CUtensorMap *map, uint64_t *bar, int c0,
+                                                      int c1, int c2, uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, "
+        "{%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "h"(cta_mask)
         : "memory");
 }
 

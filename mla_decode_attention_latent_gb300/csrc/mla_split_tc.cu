@@ -16,23 +16,27 @@
 // a 128 x 512 fp32 output accumulator fills a whole SM's tensor memory, so the
 // work of one tile is split across the two CTAs of a cluster by role:
 //
-//   score CTA (rank 0)                     value CTA (rank 1)
-//   ------------------                     ------------------
-//   Q tile [128 x 576] bf16 in TMEM        O tile [128 x 512] fp32 in TMEM
-//   TMA: page -> 9 swizzled K chunks       TMA: page -> 8 swizzled V chunks
-//   tcgen05 S = Q K^T  (ts, N = 64)        tcgen05 O += P V  (ss, N = 2 x 256)
-//   4 warps: mask + online softmax,        4 warps: zero the invalid tail rows
-//     P (bf16) and the per-row O              of V, rescale O rows when the
-//     rescale factor -> local staging         running max moved, epilogue
-//     -> one bulk copy into the peer          staged through smem
+//   score CTA (rank 0)                       value CTA (rank 1)
+//   ------------------                       ------------------
+//   Q latent [128 x 512] bf16 in TMEM,       O tile [128 x 512] fp32 in TMEM
+//     Q RoPE [128 x 64] in smem              TMA: page dims 0..511 (8 chunks)
+//   TMA: 16 KB chunk slots, each holding       into a 2-stage ring
+//     one 64-dim chunk of two pages          tcgen05 O += P V  (N = 2 x 256)
+//   tcgen05 S = Q K^T over two pages at      4 warps: zero the tail rows of V,
+//     once (N = 128: full tensor rate)         lazy O rescale, epilogue staged
+//   4 warps: mask + online softmax; P and      through smem
+//     row factors -> local staging -> one
+//     bulk copy into the value CTA
 //
-// Both CTAs read each page from global memory (the second read normally hits
-// L2).  P and the row factors (17 KB per page) are written to local shared
-// memory and pushed into the value CTA by one asynchronous bulk copy that
-// completes on the value CTA's barrier, so the softmax warps never wait on
-// cluster round trips; the value CTA's MMA commit hands the buffer back
-// through a multicast commit.  The running max is rescaled lazily: O is only
-// corrected when a page's maximum exceeds the current one by more than 2^8.
+// Loads: the score CTA's producer first streams whole pages (one contiguous
+// 72 KB each) from HBM into L2 with bulk prefetches, many pages ahead; the
+// chunk loads of both CTAs then hit L2, whose bandwidth is far above HBM's, so
+// the small shared-memory rings only have to cover L2 latency.  P and the row
+// factors (17 KB per page) go to the value CTA with one asynchronous bulk
+// copy that completes on the value CTA's barrier; the value CTA's MMA commit
+// hands the buffer back through a multicast commit.  The running max is
+// rescaled lazily: O is only corrected when a page's maximum exceeds the
+// current one by more than 2^8.
 //
 // Warp roles (192 threads): warp 0 issues TMA, warp 1 allocates TMEM and
 // issues MMAs (one elected lane), warps 2..5 are the row warps; thread t of
@@ -55,59 +59,64 @@ namespace {
 
 using namespace sm103;
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;                  // 7 warps: TMA, MMA, 4 row warps, second score-MMA issuer
 constexpr int kTileRows = 128;                 // query rows per tile = TMEM lanes
-constexpr int kKStages = 2;                    // K ring (score CTA)
-constexpr int kVStages = 2;                    // V ring (value CTA)
-constexpr int kSBufs = 3;                      // S buffers in TMEM (score CTA)
+constexpr int kKSlots = 10;                    // score CTA: 16 KB chunk slots, two rings of 5
+constexpr int kRingSlots = 5;                  // slots per score-MMA issuer's ring
+constexpr int kVStages = 2;                    // value CTA ring: whole pages (dims 0..511)
+constexpr int kSBufs = 2;                      // S buffers in TMEM (score CTA), one per step of two pages
 constexpr int kPBufs = 2;                      // P buffers (staging in the score CTA, landing in the value CTA)
 constexpr int kKChunks = kDqk / 64;            // 9 chunks of 64 dims (128 B rows)
 constexpr int kVChunks = kDv / 64;             // 8
+constexpr int kLatChunks = kDv / 64;           // 8 latent chunks: the Q part kept in TMEM
 constexpr uint32_t kChunkBytes = kPage * 128;  // 64 tokens x 128 B = 8 KB
-constexpr uint32_t kKStageBytes = kKChunks * kChunkBytes;  // 72 KB
+constexpr uint32_t kSlotBytes = 2 * kChunkBytes;          // 16 KB: one chunk of two pages (128 token rows)
 constexpr uint32_t kVStageBytes = kVChunks * kChunkBytes;  // 64 KB
 constexpr uint32_t kPBytes = kTileRows * 128;             // 16 KB: 128 rows x 64 bf16, 128B-swizzled
 constexpr uint32_t kFacOff = kPBytes;                      // then fac[128] (fp32)
 constexpr uint32_t kInvLOff = kPBytes + kTileRows * 4;     // then inv_l[128] (fp32)
 constexpr uint32_t kPMsgBytes = kPBytes + 2 * kTileRows * 4;  // 17 KB, a multiple of 1 KB
-constexpr uint32_t kQCols = kDqk / 2;                      // Q: 288 TMEM columns of bf16 pairs
+constexpr uint32_t kQCols = kDv / 2;                       // Q latent: 256 TMEM columns of bf16 pairs
 constexpr uint32_t kSCol0 = kQCols;                        // S buffers follow Q
+constexpr uint32_t kSCols = 2 * kPage;                     // an S buffer holds the scores of two pages
 constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleLog2 = 8.0f;  // lazy rescale threshold (log2 units)
+constexpr float kRescaleLog2 = 8.0f;                       // lazy rescale threshold (log2 units)
+constexpr uint32_t kAheadPages = 12;                       // pages requested into L2 ahead of their chunk loads
 constexpr uint32_t kEpiCols = 64;                          // epilogue chunk: 64 fp32 columns
 constexpr uint32_t kEpiStride = kEpiCols * 4 + 16;         // padded row stride (conflict-free v4 stores)
 
 // shared-memory layout (offsets from the 1024-byte aligned base)
-// score CTA: [K ring 2 x 72 KB][P staging 2 x 17 KB]
+// score CTA: [K rings 2 x 5 x 16 KB][Q RoPE tile 16 KB][P staging 2 x 17 KB]
 constexpr uint32_t kKRingOff = 0;
-constexpr uint32_t kStageOff = kKRingOff + kKStages * kKStageBytes;
+constexpr uint32_t kQRopeOff = kKRingOff + kKSlots * kSlotBytes;
+constexpr uint32_t kStageOff = kQRopeOff + kTileRows * 128;
 constexpr uint32_t kScoreEnd = kStageOff + kPBufs * kPMsgBytes;
 // value CTA: [V ring 2 x 64 KB][P landing 2 x 17 KB][epilogue staging 34 KB]
 constexpr uint32_t kVRingOff = 0;
 constexpr uint32_t kPBufOff = kVRingOff + kVStages * kVStageBytes;
 constexpr uint32_t kEpiOff = kPBufOff + kPBufs * kPMsgBytes;
 constexpr uint32_t kValueEnd = kEpiOff + kTileRows * kEpiStride;
-// barriers at the same offset in both CTAs (the peer arrives on them)
+// barriers at the same offset in both CTAs (the peer arrives on some of them)
 constexpr uint32_t kBarOff = ((kScoreEnd > kValueEnd ? kScoreEnd : kValueEnd) + 1023u) & ~1023u;
-static_assert(kStageOff % 1024 == 0 && kPBufOff % 1024 == 0 && kPMsgBytes % 1024 == 0, "swizzled tiles need 1 KB alignment");
+static_assert(kQRopeOff % 1024 == 0 && kStageOff % 1024 == 0 && kPBufOff % 1024 == 0 && kPMsgBytes % 1024 == 0,
+              "swizzled tiles need 1 KB alignment");
 
 enum Bar {
     // score CTA
-    B_KFULL = 0, B_KEMPTY = B_KFULL + kKStages, B_SFULL = B_KEMPTY + kKStages, B_SEMPTY = B_SFULL + kSBufs,
-    B_QFULL = B_SEMPTY + kSBufs, B_PFREE = B_QFULL + 1,
+    B_KFULL = 0, B_KEMPTY = B_KFULL + kKSlots, B_SFULL = B_KEMPTY + kKSlots, B_SEMPTY = B_SFULL + kSBufs,
+    B_QFULL = B_SEMPTY + kSBufs, B_PFREE = B_QFULL + 1, B_SREADY = B_PFREE + kPBufs,
     // value CTA
-    B_VFULL = B_PFREE + kPBufs, B_VEMPTY = B_VFULL + kVStages, B_PFULL = B_VEMPTY + kVStages,
-    B_PREADY = B_PFULL + kPBufs, B_PVDONE = B_PREADY + kPBufs, B_OEMPTY = B_PVDONE + 1,
-    B_EPI = B_OEMPTY + 1,                   // group sync of the value row warps (epilogue)
-    B_SREADY = B_EPI + 1,                   // score CTA: staging pb written by all row threads
+    B_VFULL = B_SREADY + kPBufs, B_VEMPTY = B_VFULL + kVStages, B_PFULL = B_VEMPTY + kVStages,
+    B_PREADY = B_PFULL + kPBufs, B_PVDONE = B_PREADY + kPBufs, B_OEMPTY = B_PVDONE + 1, B_EPI = B_OEMPTY + 1,
     // both
-    B_FINAL = B_SREADY + kPBufs, B_COUNT = B_FINAL + 1
+    B_FINAL = B_EPI + 1, B_COUNT = B_FINAL + 1
 };
 constexpr uint32_t kTmemSlotOff = kBarOff + B_COUNT * 8;
 constexpr uint32_t kAbortOff = kTmemSlotOff + 4;
 constexpr uint32_t kSmemUsed = kAbortOff + 4;
 constexpr size_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack of the dynamic base
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+static_assert(kRingSlots * kSBufs == kKSlots, "one K ring per score-MMA issuer");
 
 // -------------------------------------------------------------- work walk
 struct Segment {
@@ -207,74 +216,170 @@ __device__ __forceinline__ int safe_block(const DecodeParams &p, int b, int page
 }
 
 // -------------------------------------------------------------- roles
-// TMA producer (one lane): streams the part's pages through the stage ring.
-// The score CTA's producer first asks L2 for the Q rows of every segment of
-// the part, so that the row warps' Q loads at segment starts hit L2.
-__device__ void producer(const DecodeParams &p, const Ctx &c, const CUtensorMap *map, bool is_score, int part,
-                         int tile) {
-    const int stages = is_score ? kKStages : kVStages;
-    const int chunks = is_score ? kKChunks : kVChunks;
-    const uint32_t stage_bytes = is_score ? kKStageBytes : kVStageBytes;
-    const int full = is_score ? B_KFULL : B_VFULL;
-    const int empty = is_score ? B_KEMPTY : B_VEMPTY;
+// Streams the part's pages into L2 ahead of their use: one bulk prefetch of a
+// whole contiguous 72 KB page, issued by the score CTA's producer lane.
+struct PagePrefetcher {
     PartWalk walk;
     Segment s;
-    if (is_score) {
-        const int rows = min(kTileRows, p.rows - tile * kTileRows);
+    int pg;
+    bool live;
+    uint32_t issued;
+    __device__ void init(const DecodeParams &p, int part) {
         walk.init(p, part);
-        while (walk.next(p, s))
-            if (s.p1 > s.p0 && rows > 0)
-                prefetch_l2(p.q + ((size_t)s.b * p.rows + (size_t)tile * kTileRows) * kDqk, (uint32_t)rows * kDqk * 2);
+        live = walk.next(p, s);
+        pg = live ? s.p0 : 0;
+        issued = 0;
     }
+    // issue prefetches until `target` pages of the part have been requested
+    __device__ void run(const DecodeParams &p, uint32_t target) {
+        while (live && issued < target) {
+            if (pg >= s.p1) {
+                live = walk.next(p, s);
+                pg = live ? s.p0 : 0;
+                continue;
+            }
+            const int blk = p.block_table[(size_t)s.b * p.max_blocks + pg];
+            if (blk >= 0 && (int64_t)blk < p.num_blocks)
+                prefetch_l2(p.kcache + (size_t)blk * kPage * kDqk, kPage * kDqk * 2);
+            ++pg;
+            ++issued;
+        }
+    }
+};
+
+// Score-CTA TMA producer (one lane).  A step is up to two consecutive pages
+// of a segment; each of a step's 9 64-dim chunks is one 16 KB ring slot
+// holding 128 token rows (first page rows 0-63, second page rows 64-127), so
+// that one tcgen05 MMA with N = 128 covers both pages.  It first asks L2 for
+// the Q rows of every segment, then keeps whole pages streaming into L2
+// kAheadPages ahead of the chunk loads.
+__device__ void score_producer(const DecodeParams &p, const Ctx &c, const CUtensorMap *map, int part, int tile) {
+    PartWalk walk;
+    Segment s;
+    const int rows = min(kTileRows, p.rows - tile * kTileRows);
+    walk.init(p, part);
+    while (walk.next(p, s))
+        if (s.p1 > s.p0 && rows > 0)
+            prefetch_l2(p.q + ((size_t)s.b * p.rows + (size_t)tile * kTileRows) * kDqk, (uint32_t)rows * kDqk * 2);
+    PagePrefetcher ahead;
+    ahead.init(p, part);
+    ahead.run(p, kAheadPages);
+    walk.init(p, part);
+    uint32_t ring_it[kSBufs] = {0, 0};  // chunks issued into each issuer's ring
+    uint32_t step = 0, pages_done = 0;
+    bool ok = true;
+    while (ok && walk.next(p, s)) {
+        for (int pg = s.p0; ok && pg < s.p1; pg += 2, ++step) {
+            const int npg = min(2, s.p1 - pg);
+            pages_done += npg;
+            ahead.run(p, pages_done + kAheadPages);
+            const int blk0 = safe_block(p, s.b, pg);
+            const int blk1 = npg > 1 ? safe_block(p, s.b, pg + 1) : 0;
+            const int r = step % kSBufs;  // the ring of the issuer that owns this step
+            for (int ch = 0; ch < kKChunks; ++ch) {
+                const uint32_t k = ring_it[r]++;
+                const int sl = r * kRingSlots + (int)(k % kRingSlots);
+                if (!wait(c, B_KEMPTY + sl, ((k / kRingSlots) & 1) ^ 1)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *dst = c.base + kKRingOff + sl * kSlotBytes;
+                mbar_arrive_expect_tx(c.bar(B_KFULL + sl), npg * kChunkBytes);
+                tma_load_3d(dst, map, c.bar(B_KFULL + sl), 64 * ch, 0, blk0);
+                if (npg > 1) tma_load_3d(dst + kChunkBytes, map, c.bar(B_KFULL + sl), 64 * ch, 0, blk1);
+            }
+        }
+    }
+    // the last loads must have landed before this CTA may exit (already true
+    // on the normal path, where the MMAs consumed them)
+    for (int r = 0; r < kSBufs; ++r)
+        for (uint32_t k = ring_it[r] > (uint32_t)kRingSlots ? ring_it[r] - kRingSlots : 0; k < ring_it[r]; ++k)
+            mbar_wait(c.bar(B_KFULL + r * kRingSlots + (int)(k % kRingSlots)), (k / kRingSlots) & 1, c.status);
+}
+
+// Value-CTA TMA producer (one lane): whole pages (dims 0..511) through the V ring.
+__device__ void value_producer(const DecodeParams &p, const Ctx &c, const CUtensorMap *map, int part) {
+    PartWalk walk;
+    Segment s;
     walk.init(p, part);
     uint32_t it = 0;
     bool ok = true;
     while (ok && walk.next(p, s)) {
         for (int pg = s.p0; pg < s.p1; ++pg, ++it) {
-            const int st = it % stages;
-            const uint32_t use = it / stages;
-            if (!wait(c, empty + st, (use & 1) ^ 1)) {
+            const int st = it % kVStages;
+            if (!wait(c, B_VEMPTY + st, ((it / kVStages) & 1) ^ 1)) {
                 ok = false;
                 break;
             }
             const int blk = safe_block(p, s.b, pg);
-            mbar_arrive_expect_tx(c.bar(full + st), stage_bytes);
-            uint8_t *dst = c.base + st * stage_bytes;  // both rings start at offset 0
-            for (int ch = 0; ch < chunks; ++ch) tma_load_3d(dst + ch * kChunkBytes, map, c.bar(full + st), 64 * ch, 0, blk);
+            mbar_arrive_expect_tx(c.bar(B_VFULL + st), kVStageBytes);
+            uint8_t *dst = c.base + kVRingOff + st * kVStageBytes;
+            for (int ch = 0; ch < kVChunks; ++ch)
+                tma_load_3d(dst + ch * kChunkBytes, map, c.bar(B_VFULL + st), 64 * ch, 0, blk);
         }
     }
-    // the last loads must have landed before this CTA may exit (already true
-    // on the normal path, where the MMA consumed them)
-    for (uint32_t k = it > (uint32_t)stages ? it - stages : 0; k < it; ++k)
-        mbar_wait(c.bar(full + (int)(k % stages)), (k / stages) & 1, c.status);
+    for (uint32_t k = it > (uint32_t)kVStages ? it - kVStages : 0; k < it; ++k)
+        mbar_wait(c.bar(B_VFULL + (int)(k % kVStages)), (k / kVStages) & 1, c.status);
 }
 
-// Score-CTA MMA issuer: S[buf] = Q K^T for every page.
-__device__ void score_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, int part) {
-    constexpr uint32_t idesc = idesc_bf16(kTileRows, kPage, false, false);
+// Score-CTA MMA issuers: S[buf] = Q K^T for every step of (up to) two pages:
+// the 512 latent dims with A = Q from TMEM, the 64 RoPE dims with A = the
+// Q RoPE tile in shared memory; B = the 128 (or 64) token rows of each slot.
+// A tcgen05.mma holds its issuing thread for about its own execution time, so
+// whatever that thread does between MMAs (barrier waits, commits, loop
+// bookkeeping) leaves the tensor pipe idle.  Two issuers therefore alternate
+// steps by global step index (`lane` 0: even steps into S buffer 0, 1: odd
+// steps into buffer 1): one's bookkeeping overlaps the other's MMAs.  Each
+// issuer has its own ring of chunk slots, filled in step order by the
+// producer and consumed in order by its only consumer: with a shared ring, an
+// issuer could test a slot's barrier for a later phase while the other
+// issuer's earlier chunk in that slot had not landed, which parity waits
+// cannot tell apart.  Both issuers also wait for every segment's Q, so that
+// their view of the Q barrier's phases stays exact.
+__device__ void score_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, int part, int lane) {
     PartWalk walk;
     walk.init(p, part);
     Segment s;
-    uint32_t it = 0, seg = 0;
+    uint32_t step = 0, seg = 0, ring_it = 0;  // ring_it: chunks consumed from this issuer's own ring
+    const uint32_t ring = smem_u32(c.base + kKRingOff);
+    const uint64_t rope_desc = desc_sw128(smem_u32(c.base + kQRopeOff), 16, 1024);
+    const uint32_t d = tmem + kSCol0 + lane * kSCols;  // this issuer's S buffer
     while (walk.next(p, s)) {
-        if (!wait(c, B_QFULL, seg & 1)) return;  // Q of this segment is in TMEM
-        ++seg;
+        const int nsteps = (s.p1 - s.p0 + 1) / 2;
+        if (!wait(c, B_QFULL, seg & 1)) return;  // Q of this segment is in TMEM and smem
         tc_fence_after();
-        for (int pg = s.p0; pg < s.p1; ++pg, ++it) {
-            const int st = it % kKStages, sb = it % kSBufs;
-            if (!wait(c, B_KFULL + st, (it / kKStages) & 1)) return;
-            if (!wait(c, B_SEMPTY + sb, ((it / kSBufs) & 1) ^ 1)) return;
-            tc_fence_after();
-            const uint32_t ktile = smem_u32(c.base + kKRingOff + st * kKStageBytes);
-            const uint32_t d = tmem + kSCol0 + sb * kPage;
-#pragma unroll
-            for (int kk = 0; kk < kDqk / 16; ++kk) {
-                const uint64_t bd = desc_sw128(ktile + (kk / 4) * kChunkBytes + (kk % 4) * 32, 16, 1024);
-                mma_ts(d, tmem + kk * 8, bd, idesc, kk > 0);
+        ++seg;
+        for (int j = 0; j < nsteps; ++j) {
+            const uint32_t st = step + j;       // global step index
+            if ((int)(st % kSBufs) != lane) continue;
+            const int npg = min(2, s.p1 - (s.p0 + 2 * j));
+            const uint32_t idesc = npg == 2 ? idesc_bf16(kTileRows, 2 * kPage, false, false)
+                                            : idesc_bf16(kTileRows, kPage, false, false);
+            if (!wait(c, B_SEMPTY + lane, ((st / kSBufs) & 1) ^ 1)) return;
+            tc_fence_after();  // the row warps' reads of this S buffer come first
+            for (int ch = 0; ch < kKChunks; ++ch, ++ring_it) {
+                const uint32_t sl = lane * kRingSlots + ring_it % kRingSlots;
+                // TMA data: the barrier's completion already orders it before
+                // the MMA's reads (no tcgen05 fence here: it would drain the pipe)
+                if (!wait(c, B_KFULL + sl, (ring_it / kRingSlots) & 1)) return;
+                const uint64_t bd = desc_sw128(ring + sl * kSlotBytes, 16, 1024);
+                if (ch < kLatChunks) {
+                    const uint32_t a = tmem + ch * 32;
+                    mma_ts(d, a, bd, idesc, ch != 0);
+                    mma_ts(d, a + 8, bd + 2, idesc, 1u);   // +32 B along K: descriptor address field +2
+                    mma_ts(d, a + 16, bd + 4, idesc, 1u);
+                    mma_ts(d, a + 24, bd + 6, idesc, 1u);
+                } else {
+                    mma_ss(d, rope_desc, bd, idesc, 1u);
+                    mma_ss(d, rope_desc + 2, bd + 2, idesc, 1u);
+                    mma_ss(d, rope_desc + 4, bd + 4, idesc, 1u);
+                    mma_ss(d, rope_desc + 6, bd + 6, idesc, 1u);
+                }
+                mma_commit(c.bar(B_KEMPTY + sl));
             }
-            mma_commit(c.bar(B_KEMPTY + st));
-            mma_commit(c.bar(B_SFULL + sb));
+            mma_commit(c.bar(B_SFULL + lane));
         }
+        step += nsteps;
     }
 }
 
@@ -310,7 +415,8 @@ __device__ void value_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, in
     }
 }
 
-// Score-CTA row warps: Q -> TMEM, masked online softmax, P and factors -> peer.
+// Score-CTA row warps: Q -> TMEM and smem, masked online softmax, P and row
+// factors -> staging -> one bulk copy into the value CTA.
 __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, int part, int tile) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = 32 * (warp & 3) + lane;                // tile row = TMEM lane
@@ -324,20 +430,21 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
     PartWalk walk;
     walk.init(p, part);
     Segment s;
-    uint32_t it = 0;
+    uint32_t it = 0, step = 0;
     while (walk.next(p, s)) {
         const int T_row = p.causal ? s.T - p.s_q + qi + 1 : s.T;
         if (s.p1 > s.p0) {
-            // Q rows into TMEM columns [0, 288): bf16 pairs, row r in lane r;
-            // three 64-dim chunks (24 loads) in flight at a time
+            // Q row r: latent dims 0..511 into TMEM lane r (columns 0..255,
+            // bf16 pairs), RoPE dims 512..575 into row r of the swizzled smem
+            // tile; four 64-dim chunks (32 loads) in flight at a time
             const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q + ((size_t)s.b * p.rows + (row_ok ? gr : 0)) * kDqk);
 #pragma unroll 1
-            for (int ch0 = 0; ch0 < kKChunks; ch0 += 3) {
-                uint4 x[24];
+            for (int ch0 = 0; ch0 < kLatChunks; ch0 += 4) {
+                uint4 x[32];
 #pragma unroll
-                for (int j = 0; j < 24; ++j) x[j] = row_ok ? __ldg(qrow + ch0 * 8 + j) : make_uint4(0, 0, 0, 0);
+                for (int j = 0; j < 32; ++j) x[j] = row_ok ? __ldg(qrow + ch0 * 8 + j) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-                for (int k = 0; k < 3; ++k) {
+                for (int k = 0; k < 4; ++k) {
                     uint32_t v[32];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
@@ -349,6 +456,10 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
                     tmem_st32(tmem + lane_base + (ch0 + k) * 32, v);
                 }
             }
+            uint4 *rope = reinterpret_cast<uint4 *>(c.base + kQRopeOff + r * 128);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) rope[j ^ (r & 7)] = row_ok ? __ldg(qrow + kLatChunks * 8 + j) : make_uint4(0, 0, 0, 0);
+            fence_proxy_async_smem();
             tmem_wait_st();
         }
         tc_fence_before();
@@ -356,19 +467,24 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
 
         float m = -CUDART_INF_F, l = 0.f;
         for (int pg = s.p0; pg < s.p1; ++pg, ++it) {
-            const int sb = it % kSBufs, pb = it % kPBufs;
-            if (!warp_wait(c, B_SFULL + sb, (it / kSBufs) & 1)) return;
+            const int pb = it % kPBufs;
+            const int q2 = (pg - s.p0) & 1;          // position of this page in its step
+            const int sb = step % kSBufs;
+            if (q2 == 0 && !warp_wait(c, B_SFULL + sb, (step / kSBufs) & 1)) return;
             tc_fence_after();
             uint32_t sr[64];
             {
                 uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
                 uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
-                tmem_ld32(tmem + lane_base + kSCol0 + sb * kPage, lo);
-                tmem_ld32(tmem + lane_base + kSCol0 + sb * kPage + 32, hi);
+                tmem_ld32(tmem + lane_base + kSCol0 + sb * kSCols + q2 * kPage, lo);
+                tmem_ld32(tmem + lane_base + kSCol0 + sb * kSCols + q2 * kPage + 32, hi);
             }
             tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(c.bar(B_SEMPTY + sb));
+            if (q2 == 1 || pg == s.p1 - 1) {         // last page of the step: release its S buffer
+                tc_fence_before();
+                mbar_arrive(c.bar(B_SEMPTY + sb));
+                ++step;
+            }
 
             // keys of this page visible to this row
             int nvalid = row_ok ? T_row - pg * kPage : 0;
@@ -414,7 +530,8 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
             if (issuer) {
                 if (!wait(c, B_SREADY + pb, (it / kPBufs) & 1)) return;
                 const uint32_t bar = peer_pfull + pb * 8;
-                mbar_arrive_expect_tx_remote(bar, kPMsgBytes);
+                // the bulk copy's completion on the same barrier makes P visible
+                mbar_arrive_expect_tx_remote_relaxed(bar, kPMsgBytes);
                 bulk_copy_to_peer(peer_buf + pb * kPMsgBytes, stage, kPMsgBytes, bar);
             }
         }
@@ -563,6 +680,7 @@ __device__ void value_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
     }
 }
 
+
 // -------------------------------------------------------------- kernel
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p) {
@@ -583,9 +701,13 @@ split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParam
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + kTmemSlotOff);
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kKStages; ++i) {
+        for (int i = 0; i < kKSlots; ++i) {
             mbar_init(c.bar(B_KFULL + i), 1);
             mbar_init(c.bar(B_KEMPTY + i), 1);
+        }
+        for (int i = 0; i < kVStages; ++i) {
+            mbar_init(c.bar(B_VFULL + i), 1);
+            mbar_init(c.bar(B_VEMPTY + i), 1);
         }
         for (int i = 0; i < kSBufs; ++i) {
             mbar_init(c.bar(B_SFULL + i), 1);
@@ -594,18 +716,14 @@ split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParam
         mbar_init(c.bar(B_QFULL), 128);
         for (int i = 0; i < kPBufs; ++i) {
             mbar_init(c.bar(B_PFREE + i), 1);
+            mbar_init(c.bar(B_SREADY + i), 128);
             mbar_init(c.bar(B_PFULL + i), 1);
             mbar_init(c.bar(B_PREADY + i), 128);
-        }
-        for (int i = 0; i < kVStages; ++i) {
-            mbar_init(c.bar(B_VFULL + i), 1);
-            mbar_init(c.bar(B_VEMPTY + i), 1);
         }
         mbar_init(c.bar(B_PVDONE), 1);
         mbar_init(c.bar(B_OEMPTY), 128);
         mbar_init(c.bar(B_EPI), 128);
-        for (int i = 0; i < kPBufs; ++i) mbar_init(c.bar(B_SREADY + i), 128);
-        mbar_init(c.bar(B_FINAL), 1);
+        mbar_init(c.bar(B_FINAL), is_score ? 2 : 1);  // one commit per MMA issuer
         *c.abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&kv_map);
@@ -622,10 +740,13 @@ split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParam
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        if (elect_one_lane()) producer(p, c, &kv_map, is_score, part, tile);
-    } else if (warp == 1) {
         if (elect_one_lane()) {
-            if (is_score) score_mma(p, c, tmem, part);
+            if (is_score) score_producer(p, c, &kv_map, part, tile);
+            else value_producer(p, c, &kv_map, part);
+        }
+    } else if (warp == 1 || warp == 6) {
+        if (elect_one_lane() && (warp == 1 || is_score)) {
+            if (is_score) score_mma(p, c, tmem, part, warp == 1 ? 0 : 1);
             else value_mma(p, c, tmem, part);
             // all MMAs this thread issued must finish before TMEM is released
             mma_commit(c.bar(B_FINAL));
