@@ -38,9 +38,10 @@
 // rescaled lazily: O is only corrected when a page's maximum exceeds the
 // current one by more than 2^8.
 //
-// Warp roles (192 threads): warp 0 issues TMA, warp 1 allocates TMEM and
-// issues MMAs (one elected lane), warps 2..5 are the row warps; thread t of
-// warp w owns TMEM lane / tile row 32 * (w % 4) + t.
+// Warp roles (256 threads): warp 0 issues TMA, warp 1 allocates TMEM and
+// issues MMAs (one elected lane), warps 2..5 are the row warps (thread t of
+// warp w owns TMEM lane / tile row 32 * (w % 4) + t); in the score CTA warp 6
+// is the second MMA issuer and warp 7 the second TMA producer.
 //
 // Every wait is bounded (mla_sm103.cuh); on a timeout the kernel raises
 // MLA_DEVERR_TIMEOUT, tells its peer CTA to stop, and unwinds.
@@ -59,13 +60,14 @@ namespace {
 
 using namespace sm103;
 
-constexpr int kThreads = 224;                  // 7 warps: TMA, MMA, 4 row warps, second score-MMA issuer
+constexpr int kThreads = 256;                  // 8 warps: TMA, MMA, 4 row warps, second score MMA issuer and TMA producer
 constexpr int kTileRows = 128;                 // query rows per tile = TMEM lanes
 constexpr int kKSlots = 10;                    // score CTA: 16 KB chunk slots, two rings of 5
 constexpr int kRingSlots = 5;                  // slots per score-MMA issuer's ring
 constexpr int kVStages = 2;                    // value CTA ring: whole pages (dims 0..511)
 constexpr int kSBufs = 2;                      // S buffers in TMEM (score CTA), one per step of two pages
 constexpr int kPBufs = 2;                      // P buffers (staging in the score CTA, landing in the value CTA)
+constexpr int kScoreIssuers = 2;               // score-CTA MMA issuers, alternating steps
 constexpr int kKChunks = kDqk / 64;            // 9 chunks of 64 dims (128 B rows)
 constexpr int kVChunks = kDv / 64;             // 8
 constexpr int kLatChunks = kDv / 64;           // 8 latent chunks: the Q part kept in TMEM
@@ -104,10 +106,11 @@ static_assert(kQRopeOff % 1024 == 0 && kStageOff % 1024 == 0 && kPBufOff % 1024 
 enum Bar {
     // score CTA
     B_KFULL = 0, B_KEMPTY = B_KFULL + kKSlots, B_SFULL = B_KEMPTY + kKSlots, B_SEMPTY = B_SFULL + kSBufs,
-    B_QFULL = B_SEMPTY + kSBufs, B_PFREE = B_QFULL + 1, B_SREADY = B_PFREE + kPBufs,
+    B_QFULL = B_SEMPTY + kSBufs, B_QACK = B_QFULL + 1, B_PFREE = B_QACK + 1, B_SREADY = B_PFREE + kPBufs,
     // value CTA
     B_VFULL = B_SREADY + kPBufs, B_VEMPTY = B_VFULL + kVStages, B_PFULL = B_VEMPTY + kVStages,
-    B_PREADY = B_PFULL + kPBufs, B_PVDONE = B_PREADY + kPBufs, B_OEMPTY = B_PVDONE + 1, B_EPI = B_OEMPTY + 1,
+    B_PREADY = B_PFULL + kPBufs, B_PVDONE = B_PREADY + kPBufs, B_ODONE = B_PVDONE + 1, B_OEMPTY = B_ODONE + 1,
+    B_EPI = B_OEMPTY + 1,
     // both
     B_FINAL = B_EPI + 1, B_COUNT = B_FINAL + 1
 };
@@ -116,7 +119,7 @@ constexpr uint32_t kAbortOff = kTmemSlotOff + 4;
 constexpr uint32_t kSmemUsed = kAbortOff + 4;
 constexpr size_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack of the dynamic base
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-static_assert(kRingSlots * kSBufs == kKSlots, "one K ring per score-MMA issuer");
+static_assert(kRingSlots * kScoreIssuers == kKSlots && kSBufs == kScoreIssuers, "one K ring and one S buffer per score-MMA issuer");
 
 // -------------------------------------------------------------- work walk
 struct Segment {
@@ -247,37 +250,41 @@ struct PagePrefetcher {
     }
 };
 
-// Score-CTA TMA producer (one lane).  A step is up to two consecutive pages
+// Score-CTA TMA producers (one lane each, one per MMA issuer's ring `r`,
+// taking the steps of parity r).  A step is up to two consecutive pages
 // of a segment; each of a step's 9 64-dim chunks is one 16 KB ring slot
 // holding 128 token rows (first page rows 0-63, second page rows 64-127), so
 // that one tcgen05 MMA with N = 128 covers both pages.  It first asks L2 for
 // the Q rows of every segment, then keeps whole pages streaming into L2
 // kAheadPages ahead of the chunk loads.
-__device__ void score_producer(const DecodeParams &p, const Ctx &c, const CUtensorMap *map, int part, int tile) {
+__device__ void score_producer(const DecodeParams &p, const Ctx &c, const CUtensorMap *map, int part, int tile,
+                               int r) {
     PartWalk walk;
     Segment s;
-    const int rows = min(kTileRows, p.rows - tile * kTileRows);
-    walk.init(p, part);
-    while (walk.next(p, s))
-        if (s.p1 > s.p0 && rows > 0)
-            prefetch_l2(p.q + ((size_t)s.b * p.rows + (size_t)tile * kTileRows) * kDqk, (uint32_t)rows * kDqk * 2);
     PagePrefetcher ahead;
-    ahead.init(p, part);
-    ahead.run(p, kAheadPages);
+    if (r == 0) {
+        const int rows = min(kTileRows, p.rows - tile * kTileRows);
+        walk.init(p, part);
+        while (walk.next(p, s))
+            if (s.p1 > s.p0 && rows > 0)
+                prefetch_l2(p.q + ((size_t)s.b * p.rows + (size_t)tile * kTileRows) * kDqk, (uint32_t)rows * kDqk * 2);
+        ahead.init(p, part);
+        ahead.run(p, kAheadPages);
+    }
     walk.init(p, part);
-    uint32_t ring_it[kSBufs] = {0, 0};  // chunks issued into each issuer's ring
+    uint32_t ring_it = 0;  // chunks issued into this producer's ring
     uint32_t step = 0, pages_done = 0;
     bool ok = true;
     while (ok && walk.next(p, s)) {
         for (int pg = s.p0; ok && pg < s.p1; pg += 2, ++step) {
             const int npg = min(2, s.p1 - pg);
             pages_done += npg;
-            ahead.run(p, pages_done + kAheadPages);
+            if ((int)(step % kSBufs) != r) continue;  // the other ring's step
+            if (r == 0) ahead.run(p, pages_done + kAheadPages);
             const int blk0 = safe_block(p, s.b, pg);
             const int blk1 = npg > 1 ? safe_block(p, s.b, pg + 1) : 0;
-            const int r = step % kSBufs;  // the ring of the issuer that owns this step
             for (int ch = 0; ch < kKChunks; ++ch) {
-                const uint32_t k = ring_it[r]++;
+                const uint32_t k = ring_it++;
                 const int sl = r * kRingSlots + (int)(k % kRingSlots);
                 if (!wait(c, B_KEMPTY + sl, ((k / kRingSlots) & 1) ^ 1)) {
                     ok = false;
@@ -292,9 +299,8 @@ __device__ void score_producer(const DecodeParams &p, const Ctx &c, const CUtens
     }
     // the last loads must have landed before this CTA may exit (already true
     // on the normal path, where the MMAs consumed them)
-    for (int r = 0; r < kSBufs; ++r)
-        for (uint32_t k = ring_it[r] > (uint32_t)kRingSlots ? ring_it[r] - kRingSlots : 0; k < ring_it[r]; ++k)
-            mbar_wait(c.bar(B_KFULL + r * kRingSlots + (int)(k % kRingSlots)), (k / kRingSlots) & 1, c.status);
+    for (uint32_t k = ring_it > (uint32_t)kRingSlots ? ring_it - kRingSlots : 0; k < ring_it; ++k)
+        mbar_wait(c.bar(B_KFULL + r * kRingSlots + (int)(k % kRingSlots)), (k / kRingSlots) & 1, c.status);
 }
 
 // Value-CTA TMA producer (one lane): whole pages (dims 0..511) through the V ring.
@@ -348,6 +354,7 @@ __device__ void score_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, in
         const int nsteps = (s.p1 - s.p0 + 1) / 2;
         if (!wait(c, B_QFULL, seg & 1)) return;  // Q of this segment is in TMEM and smem
         tc_fence_after();
+        mbar_arrive(c.bar(B_QACK));              // the row warps may load the next Q only after both issuers saw this one
         ++seg;
         for (int j = 0; j < nsteps; ++j) {
             const uint32_t st = step + j;       // global step index
@@ -383,16 +390,20 @@ __device__ void score_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, in
     }
 }
 
-// Value-CTA MMA issuer: O (+)= P V for every page.
+// Value-CTA MMA issuer: O (+)= P V for every page.  Only segments with pages
+// touch O, so only they count on the O barriers: the epilogue of a segment
+// without pages never waits on this thread, and counting it would let the row
+// warps complete two phases of the O-free barrier between two of its waits.
 __device__ void value_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, int part) {
     constexpr uint32_t idesc = idesc_bf16(kTileRows, 256, false, true);
     PartWalk walk;
     walk.init(p, part);
     Segment s;
-    uint32_t it = 0, seg = 0;
+    uint32_t it = 0, oseg = 0;  // oseg: segments with pages so far
     while (walk.next(p, s)) {
-        if (!wait(c, B_OEMPTY, (seg & 1) ^ 1)) return;  // previous segment's epilogue has read O
-        ++seg;
+        if (s.p1 <= s.p0) continue;
+        if (!wait(c, B_OEMPTY, (oseg & 1) ^ 1)) return;  // previous segment's epilogue has read O
+        ++oseg;
         for (int pg = s.p0; pg < s.p1; ++pg, ++it) {
             const int st = it % kVStages, pb = it % kPBufs;
             if (!wait(c, B_VFULL + st, (it / kVStages) & 1)) return;
@@ -410,6 +421,7 @@ __device__ void value_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, in
                 }
             mma_commit(c.bar(B_VEMPTY + st));
             mma_commit(c.bar(B_PVDONE));
+            if (pg == s.p1 - 1) mma_commit(c.bar(B_ODONE));  // O of the segment is complete
             mma_commit_multicast(c.bar(B_PFREE + pb), (uint16_t)(1u << c.peer));
         }
     }
@@ -430,9 +442,13 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
     PartWalk walk;
     walk.init(p, part);
     Segment s;
-    uint32_t it = 0, step = 0;
+    uint32_t it = 0, step = 0, seg = 0;
     while (walk.next(p, s)) {
         const int T_row = p.causal ? s.T - p.s_q + qi + 1 : s.T;
+        // both MMA issuers have seen the previous segment's Q (and, having
+        // consumed all its S buffers, the MMAs reading it are done)
+        if (seg > 0 && !warp_wait(c, B_QACK, (seg - 1) & 1)) return;
+        ++seg;
         if (s.p1 > s.p0) {
             // Q row r: latent dims 0..511 into TMEM lane r (columns 0..255,
             // bf16 pairs), RoPE dims 512..575 into row r of the swizzled smem
@@ -489,19 +505,31 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
             // keys of this page visible to this row
             int nvalid = row_ok ? T_row - pg * kPage : 0;
             nvalid = nvalid < 0 ? 0 : (nvalid > kPage ? kPage : nvalid);
+            const float sc = p.scale_log2;
             float x[64];
-            float mx = -CUDART_INF_F;
+            // page maximum of scale * log2(e) * s over the visible keys, four
+            // independent chains to keep the dependency depth short
+            float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
+            if (nvalid == kPage) {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                x[j] = (j < nvalid) ? __uint_as_float(sr[j]) * p.scale_log2 : -CUDART_INF_F;
-                mx = fmaxf(mx, x[j]);
+                for (int j = 0; j < 64; ++j) {
+                    x[j] = __uint_as_float(sr[j]) * sc;
+                    mx4[j & 3] = fmaxf(mx4[j & 3], x[j]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    x[j] = (j < nvalid) ? __uint_as_float(sr[j]) * sc : -CUDART_INF_F;
+                    mx4[j & 3] = fmaxf(mx4[j & 3], x[j]);
+                }
             }
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
             float fac = 1.f;
             if (mx > m + kRescaleLog2 || (m == -CUDART_INF_F && mx > -CUDART_INF_F)) {
                 fac = ex2(m - mx);  // 0 when m was -inf
                 m = mx;
             }
-            float sum = 0.f;
+            float sum4[4] = {0.f, 0.f, 0.f, 0.f};
             uint32_t pk[32];
             if (m == -CUDART_INF_F) {
 #pragma unroll
@@ -510,10 +538,11 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const float a = ex2(x[2 * j] - m), b = ex2(x[2 * j + 1] - m);
-                    sum += a + b;
+                    sum4[j & 3] += a + b;
                     pk[j] = pack_bf16(a, b);
                 }
             }
+            const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
             l = l * fac + sum;
 
             // staging pb is free once the value CTA's MMA of page it - 2 is
@@ -564,7 +593,7 @@ __device__ void value_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
     PartWalk walk;
     walk.init(p, part);
     Segment s;
-    uint32_t it = 0;
+    uint32_t it = 0, oseg = 0;  // oseg: segments with pages so far
     while (walk.next(p, s)) {
         float inv_l = 0.f;
         for (int pg = s.p0; pg < s.p1; ++pg, ++it) {
@@ -612,7 +641,12 @@ __device__ void value_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
         // thread), then every warp writes 32 whole rows with coalesced stores.
         const bool has_pages = s.p1 > s.p0;
         if (has_pages) {
-            if (!warp_wait(c, B_PVDONE, (it - 1) & 1)) return;
+            // every P V of the segment has landed.  (The per-page barrier
+            // cannot serve here: the row warps only know that the MMA of page
+            // it - 3 is done, and a parity wait cannot tell phase it - 1 from
+            // phase it - 3.)
+            if (!warp_wait(c, B_ODONE, oseg & 1)) return;
+            ++oseg;
             tc_fence_after();
         }
         const bool split = s.n_split > 1;
@@ -675,8 +709,10 @@ __device__ void value_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
             }
             if (!group_sync(c, B_EPI, epi_phase)) return;
         }
-        tc_fence_before();
-        mbar_arrive(c.bar(B_OEMPTY));
+        if (has_pages) {
+            tc_fence_before();
+            mbar_arrive(c.bar(B_OEMPTY));
+        }
     }
 }
 
@@ -714,6 +750,7 @@ split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParam
             mbar_init(c.bar(B_SEMPTY + i), 128);
         }
         mbar_init(c.bar(B_QFULL), 128);
+        mbar_init(c.bar(B_QACK), kScoreIssuers);  // every score-MMA issuer has seen a segment's Q
         for (int i = 0; i < kPBufs; ++i) {
             mbar_init(c.bar(B_PFREE + i), 1);
             mbar_init(c.bar(B_SREADY + i), 128);
@@ -721,6 +758,7 @@ split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParam
             mbar_init(c.bar(B_PREADY + i), 128);
         }
         mbar_init(c.bar(B_PVDONE), 1);
+        mbar_init(c.bar(B_ODONE), 1);
         mbar_init(c.bar(B_OEMPTY), 128);
         mbar_init(c.bar(B_EPI), 128);
         mbar_init(c.bar(B_FINAL), is_score ? 2 : 1);  // one commit per MMA issuer
@@ -739,9 +777,9 @@ split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParam
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        if (elect_one_lane()) {
-            if (is_score) score_producer(p, c, &kv_map, part, tile);
+    if (warp == 0 || warp == 7) {
+        if (elect_one_lane() && (warp == 0 || is_score)) {
+            if (is_score) score_producer(p, c, &kv_map, part, tile, warp == 0 ? 0 : 1);
             else value_producer(p, c, &kv_map, part);
         }
     } else if (warp == 1 || warp == 6) {
