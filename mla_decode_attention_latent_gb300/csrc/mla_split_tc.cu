@@ -63,11 +63,11 @@ using namespace sm103;
 constexpr int kThreads = 256;                  // 8 warps: TMA, MMA, 4 row warps, second score MMA issuer and TMA producer
 constexpr int kTileRows = 128;                 // query rows per tile = TMEM lanes
 constexpr int kKSlots = 10;                    // score CTA: 16 KB chunk slots, two rings of 5
-constexpr int kRingSlots = 5;                  // slots per score-MMA issuer's ring
+constexpr int kScoreIssuers = 2;               // score-CTA MMA issuers (and TMA producers), alternating steps
+constexpr int kRingSlots = 10 / kScoreIssuers;  // slots per score-MMA issuer's ring
 constexpr int kVStages = 2;                    // value CTA ring: whole pages (dims 0..511)
 constexpr int kSBufs = 2;                      // S buffers in TMEM (score CTA), one per step of two pages
 constexpr int kPBufs = 2;                      // P buffers (staging in the score CTA, landing in the value CTA)
-constexpr int kScoreIssuers = 2;               // score-CTA MMA issuers, alternating steps
 constexpr int kKChunks = kDqk / 64;            // 9 chunks of 64 dims (128 B rows)
 constexpr int kVChunks = kDv / 64;             // 8
 constexpr int kLatChunks = kDv / 64;           // 8 latent chunks: the Q part kept in TMEM
@@ -83,7 +83,8 @@ constexpr uint32_t kSCol0 = kQCols;                        // S buffers follow Q
 constexpr uint32_t kSCols = 2 * kPage;                     // an S buffer holds the scores of two pages
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;                       // lazy rescale threshold (log2 units)
-constexpr uint32_t kAheadPages = 12;                       // pages requested into L2 ahead of their chunk loads
+constexpr uint32_t kScoreAheadPages = 0;                   // pages the score CTA requests into L2 ahead of its loads
+constexpr uint32_t kValueAheadPages = 0;                   // pages the value CTA requests into L2 ahead of its loads
 constexpr uint32_t kEpiCols = 64;                          // epilogue chunk: 64 fp32 columns
 constexpr uint32_t kEpiStride = kEpiCols * 4 + 16;         // padded row stride (conflict-free v4 stores)
 
@@ -106,9 +107,9 @@ static_assert(kQRopeOff % 1024 == 0 && kStageOff % 1024 == 0 && kPBufOff % 1024 
 enum Bar {
     // score CTA
     B_KFULL = 0, B_KEMPTY = B_KFULL + kKSlots, B_SFULL = B_KEMPTY + kKSlots, B_SEMPTY = B_SFULL + kSBufs,
-    B_QFULL = B_SEMPTY + kSBufs, B_QACK = B_QFULL + 1, B_PFREE = B_QACK + 1, B_SREADY = B_PFREE + kPBufs,
+    B_QFULL = B_SEMPTY + kSBufs, B_QACK = B_QFULL + 1, B_PFREE = B_QACK + 1,
     // value CTA
-    B_VFULL = B_SREADY + kPBufs, B_VEMPTY = B_VFULL + kVStages, B_PFULL = B_VEMPTY + kVStages,
+    B_VFULL = B_PFREE + kPBufs, B_VEMPTY = B_VFULL + kVStages, B_PFULL = B_VEMPTY + kVStages,
     B_PREADY = B_PFULL + kPBufs, B_PVDONE = B_PREADY + kPBufs, B_ODONE = B_PVDONE + 1, B_OEMPTY = B_ODONE + 1,
     B_EPI = B_OEMPTY + 1,
     // both
@@ -119,7 +120,7 @@ constexpr uint32_t kAbortOff = kTmemSlotOff + 4;
 constexpr uint32_t kSmemUsed = kAbortOff + 4;
 constexpr size_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack of the dynamic base
 static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-static_assert(kRingSlots * kScoreIssuers == kKSlots && kSBufs == kScoreIssuers, "one K ring and one S buffer per score-MMA issuer");
+static_assert(kRingSlots * kScoreIssuers == kKSlots && kSBufs % kScoreIssuers == 0, "one K ring per score-MMA issuer");
 
 // -------------------------------------------------------------- work walk
 struct Segment {
@@ -254,9 +255,10 @@ struct PagePrefetcher {
 // taking the steps of parity r).  A step is up to two consecutive pages
 // of a segment; each of a step's 9 64-dim chunks is one 16 KB ring slot
 // holding 128 token rows (first page rows 0-63, second page rows 64-127), so
-// that one tcgen05 MMA with N = 128 covers both pages.  It first asks L2 for
-// the Q rows of every segment, then keeps whole pages streaming into L2
-// kAheadPages ahead of the chunk loads.
+// that one tcgen05 MMA with N = 128 covers both pages.  Producer 0 first asks
+// L2 for the Q rows of every segment.  (Streaming whole pages into L2 ahead
+// of the chunk loads, from either CTA, measured slower on GB300 at every
+// distance tried, so both distances are 0.)
 __device__ void score_producer(const DecodeParams &p, const Ctx &c, const CUtensorMap *map, int part, int tile,
                                int r) {
     PartWalk walk;
@@ -268,8 +270,10 @@ __device__ void score_producer(const DecodeParams &p, const Ctx &c, const CUtens
         while (walk.next(p, s))
             if (s.p1 > s.p0 && rows > 0)
                 prefetch_l2(p.q + ((size_t)s.b * p.rows + (size_t)tile * kTileRows) * kDqk, (uint32_t)rows * kDqk * 2);
-        ahead.init(p, part);
-        ahead.run(p, kAheadPages);
+        if (kScoreAheadPages > 0) {
+            ahead.init(p, part);
+            ahead.run(p, kScoreAheadPages);
+        }
     }
     walk.init(p, part);
     uint32_t ring_it = 0;  // chunks issued into this producer's ring
@@ -279,8 +283,8 @@ __device__ void score_producer(const DecodeParams &p, const Ctx &c, const CUtens
         for (int pg = s.p0; ok && pg < s.p1; pg += 2, ++step) {
             const int npg = min(2, s.p1 - pg);
             pages_done += npg;
-            if ((int)(step % kSBufs) != r) continue;  // the other ring's step
-            if (r == 0) ahead.run(p, pages_done + kAheadPages);
+            if ((int)(step % kScoreIssuers) != r) continue;  // the other ring's step
+            if (kScoreAheadPages > 0 && r == 0) ahead.run(p, pages_done + kScoreAheadPages);
             const int blk0 = safe_block(p, s.b, pg);
             const int blk1 = npg > 1 ? safe_block(p, s.b, pg + 1) : 0;
             for (int ch = 0; ch < kKChunks; ++ch) {
@@ -307,12 +311,18 @@ __device__ void score_producer(const DecodeParams &p, const Ctx &c, const CUtens
 __device__ void value_producer(const DecodeParams &p, const Ctx &c, const CUtensorMap *map, int part) {
     PartWalk walk;
     Segment s;
+    PagePrefetcher ahead;
+    if (kValueAheadPages > 0) {
+        ahead.init(p, part);
+        ahead.run(p, kValueAheadPages);
+    }
     walk.init(p, part);
     uint32_t it = 0;
     bool ok = true;
     while (ok && walk.next(p, s)) {
         for (int pg = s.p0; pg < s.p1; ++pg, ++it) {
             const int st = it % kVStages;
+            if (kValueAheadPages > 0) ahead.run(p, it + 1 + kValueAheadPages);
             if (!wait(c, B_VEMPTY + st, ((it / kVStages) & 1) ^ 1)) {
                 ok = false;
                 break;
@@ -349,7 +359,6 @@ __device__ void score_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, in
     uint32_t step = 0, seg = 0, ring_it = 0;  // ring_it: chunks consumed from this issuer's own ring
     const uint32_t ring = smem_u32(c.base + kKRingOff);
     const uint64_t rope_desc = desc_sw128(smem_u32(c.base + kQRopeOff), 16, 1024);
-    const uint32_t d = tmem + kSCol0 + lane * kSCols;  // this issuer's S buffer
     while (walk.next(p, s)) {
         const int nsteps = (s.p1 - s.p0 + 1) / 2;
         if (!wait(c, B_QFULL, seg & 1)) return;  // Q of this segment is in TMEM and smem
@@ -358,11 +367,13 @@ __device__ void score_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, in
         ++seg;
         for (int j = 0; j < nsteps; ++j) {
             const uint32_t st = step + j;       // global step index
-            if ((int)(st % kSBufs) != lane) continue;
+            if ((int)(st % kScoreIssuers) != lane) continue;
+            const int sb = (int)(st % kSBufs);
+            const uint32_t d = tmem + kSCol0 + sb * kSCols;
             const int npg = min(2, s.p1 - (s.p0 + 2 * j));
             const uint32_t idesc = npg == 2 ? idesc_bf16(kTileRows, 2 * kPage, false, false)
                                             : idesc_bf16(kTileRows, kPage, false, false);
-            if (!wait(c, B_SEMPTY + lane, ((st / kSBufs) & 1) ^ 1)) return;
+            if (!wait(c, B_SEMPTY + sb, ((st / kSBufs) & 1) ^ 1)) return;
             tc_fence_after();  // the row warps' reads of this S buffer come first
             for (int ch = 0; ch < kKChunks; ++ch, ++ring_it) {
                 const uint32_t sl = lane * kRingSlots + ring_it % kRingSlots;
@@ -384,7 +395,7 @@ __device__ void score_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, in
                 }
                 mma_commit(c.bar(B_KEMPTY + sl));
             }
-            mma_commit(c.bar(B_SFULL + lane));
+            mma_commit(c.bar(B_SFULL + sb));
         }
         step += nsteps;
     }
@@ -428,7 +439,8 @@ __device__ void value_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, in
 }
 
 // Score-CTA row warps: Q -> TMEM and smem, masked online softmax, P and row
-// factors -> staging -> one bulk copy into the value CTA.
+// factors -> staging -> bulk copies into the value CTA, each warp sending its
+// own 32 rows as soon as they are staged.
 __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, int part, int tile) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = 32 * (warp & 3) + lane;                // tile row = TMEM lane
@@ -436,7 +448,6 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
     const int gr = tile * kTileRows + r;                 // row within the sequence's rows
     const bool row_ok = gr < p.rows;
     const int qi = row_ok ? gr / p.h_q : 0;              // query token index
-    const bool issuer = threadIdx.x == 64;               // pushes each page to the peer
     const uint32_t peer_buf = mapa(smem_u32(c.base + kPBufOff), c.peer);
     const uint32_t peer_pfull = mapa(smem_u32(c.bar(B_PFULL)), c.peer);
     PartWalk walk;
@@ -506,24 +517,27 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
             int nvalid = row_ok ? T_row - pg * kPage : 0;
             nvalid = nvalid < 0 ? 0 : (nvalid > kPage ? kPage : nvalid);
             const float sc = p.scale_log2;
-            float x[64];
             // page maximum of scale * log2(e) * s over the visible keys, four
-            // independent chains to keep the dependency depth short
+            // independent chains to keep the dependency depth short.  A full
+            // page with a positive scale takes the maximum of the raw scores
+            // (scaling is monotone there) and folds the scale into one FMA per
+            // exponent below; otherwise the scaled, masked scores (-inf past
+            // the visible keys) replace the raw ones and the FMA scale is 1.
+            const bool raw = nvalid == kPage && sc > 0.f;
+            const float fsc = raw ? sc : 1.f;
             float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
-            if (nvalid == kPage) {
+            if (raw) {
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    x[j] = __uint_as_float(sr[j]) * sc;
-                    mx4[j & 3] = fmaxf(mx4[j & 3], x[j]);
-                }
+                for (int j = 0; j < 64; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(sr[j]));
             } else {
 #pragma unroll
                 for (int j = 0; j < 64; ++j) {
-                    x[j] = (j < nvalid) ? __uint_as_float(sr[j]) * sc : -CUDART_INF_F;
-                    mx4[j & 3] = fmaxf(mx4[j & 3], x[j]);
+                    const float xs = (j < nvalid) ? __uint_as_float(sr[j]) * sc : -CUDART_INF_F;
+                    sr[j] = __float_as_uint(xs);
+                    mx4[j & 3] = fmaxf(mx4[j & 3], xs);
                 }
             }
-            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * fsc;
             float fac = 1.f;
             if (mx > m + kRescaleLog2 || (m == -CUDART_INF_F && mx > -CUDART_INF_F)) {
                 fac = ex2(m - mx);  // 0 when m was -inf
@@ -535,9 +549,11 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
 #pragma unroll
                 for (int j = 0; j < 32; ++j) pk[j] = 0u;
             } else {
+                const float nm = -m;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    const float a = ex2(x[2 * j] - m), b = ex2(x[2 * j + 1] - m);
+                    const float a = ex2(fmaf(__uint_as_float(sr[2 * j]), fsc, nm));
+                    const float b = ex2(fmaf(__uint_as_float(sr[2 * j + 1]), fsc, nm));
                     sum4[j & 3] += a + b;
                     pk[j] = pack_bf16(a, b);
                 }
@@ -555,13 +571,18 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
             reinterpret_cast<float *>(stage + kFacOff)[r] = fac;
             if (pg == s.p1 - 1) reinterpret_cast<float *>(stage + kInvLOff)[r] = l > 0.f ? 1.f / l : 0.f;
             fence_proxy_async_smem();
-            mbar_arrive(c.bar(B_SREADY + pb));
-            if (issuer) {
-                if (!wait(c, B_SREADY + pb, (it / kPBufs) & 1)) return;
+            __syncwarp();
+            if (lane == 0) {
+                // this warp's 32 rows of P and of the row factors; the bulk
+                // copies' completion on the same barrier makes them visible
+                const bool last = pg == s.p1 - 1;
                 const uint32_t bar = peer_pfull + pb * 8;
-                // the bulk copy's completion on the same barrier makes P visible
-                mbar_arrive_expect_tx_remote_relaxed(bar, kPMsgBytes);
-                bulk_copy_to_peer(peer_buf + pb * kPMsgBytes, stage, kPMsgBytes, bar);
+                const uint32_t rows_off = (uint32_t)(32 * (warp & 3)) * 128, fac_off = (uint32_t)(32 * (warp & 3)) * 4;
+                const uint32_t dst = peer_buf + pb * kPMsgBytes;
+                mbar_arrive_expect_tx_remote_relaxed(bar, 32 * 128 + (last ? 2 : 1) * 32 * 4);
+                bulk_copy_to_peer(dst + rows_off, stage + rows_off, 32 * 128, bar);
+                bulk_copy_to_peer(dst + kFacOff + fac_off, stage + kFacOff + fac_off, 32 * 4, bar);
+                if (last) bulk_copy_to_peer(dst + kInvLOff + fac_off, stage + kInvLOff + fac_off, 32 * 4, bar);
             }
         }
         // LSE of this row over the segment (natural log)
@@ -753,15 +774,14 @@ split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParam
         mbar_init(c.bar(B_QACK), kScoreIssuers);  // every score-MMA issuer has seen a segment's Q
         for (int i = 0; i < kPBufs; ++i) {
             mbar_init(c.bar(B_PFREE + i), 1);
-            mbar_init(c.bar(B_SREADY + i), 128);
-            mbar_init(c.bar(B_PFULL + i), 1);
+            mbar_init(c.bar(B_PFULL + i), 4);  // one arrival per row warp of the score CTA
             mbar_init(c.bar(B_PREADY + i), 128);
         }
         mbar_init(c.bar(B_PVDONE), 1);
         mbar_init(c.bar(B_ODONE), 1);
         mbar_init(c.bar(B_OEMPTY), 128);
         mbar_init(c.bar(B_EPI), 128);
-        mbar_init(c.bar(B_FINAL), is_score ? 2 : 1);  // one commit per MMA issuer
+        mbar_init(c.bar(B_FINAL), is_score ? kScoreIssuers : 1);  // one commit per MMA issuer
         *c.abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&kv_map);
@@ -778,12 +798,12 @@ split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParam
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0 || warp == 7) {
-        if (elect_one_lane() && (warp == 0 || is_score)) {
+        if (elect_one_lane() && (warp == 0 || (is_score && kScoreIssuers > 1))) {
             if (is_score) score_producer(p, c, &kv_map, part, tile, warp == 0 ? 0 : 1);
             else value_producer(p, c, &kv_map, part);
         }
     } else if (warp == 1 || warp == 6) {
-        if (elect_one_lane() && (warp == 1 || is_score)) {
+        if (elect_one_lane() && (warp == 1 || (is_score && kScoreIssuers > 1))) {
             if (is_score) score_mma(p, c, tmem, part, warp == 1 ? 0 : 1);
             else value_mma(p, c, tmem, part);
             // all MMAs this thread issued must finish before TMEM is released

@@ -129,6 +129,36 @@ def test_deterministic():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+def test_empty_segments_between_full_ones():
+    # parts that walk several sequences, some of length zero, between
+    # sequences that end in a partial page: the value side's O hand-off only
+    # counts segments with pages
+    sl = [0, 130, 0, 0, 64, 1, 0, 700, 0, 129, 63, 0]
+    c = case("empty-mix", len(sl), 2, 64, sl, causal=True, seed=111)
+    for parts in (1, 2, 3):
+        o, lse = check(c, num_parts=parts)
+        for _ in range(3):
+            o2, l2, *_ = run_gpu(to_device(W.make_inputs(c, "cpu"), DEV), num_parts=parts)
+            assert torch.equal(o, o2) and torch.equal(lse, l2), parts
+
+
+@pytest.mark.parametrize("name", ["uniform", "variable", "mtp", "long"])
+def test_full_size_repeatable(name):
+    # bit-identical outputs over repeated launches at full size: every wait
+    # on the hand-offs between the two CTAs of a pair has to be exact
+    c = W.CASES[name]
+    x = W.make_inputs(c, device="cuda")
+    o1, l1, _, _, st = run_gpu(x)
+    assert st == 0, f"device status {st:#x}"
+    for rep in range(4):
+        o2, l2, _, _, st = run_gpu(x)
+        assert st == 0, f"device status {st:#x}"
+        n_o = int((o1.view(torch.int16) != o2.view(torch.int16)).sum())
+        assert n_o == 0 and torch.equal(l1, l2), f"repeat {rep}: {n_o} O elements differ"
+    del x, o1, l1, o2, l2
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("name", ["uniform", "variable", "mtp", "long"])
 def test_full_size_sampled(name):
     c = W.CASES[name]
