@@ -13,18 +13,23 @@
 // that part) carry weight 0; a row with no visible key anywhere gets O = 0 and
 // L = -inf.
 //
-// One warp per (sequence, row).  Each lane owns 16 of the 512 output dims as
-// four float4 groups at lane*4 + 128*k, so every warp load is 512 contiguous
-// bytes.  Memory-bound: reads k * 2 KB of partials, writes 1 KB of bf16.
+// One warp per (sequence, row).  Lane s holds the partial LSE of partial s,
+// so the LSEs are read once; the weights travel by shuffle.  Each lane owns
+// 16 of the 512 output dims as four float4 groups at lane*4 + 128*k, so every
+// warp load is 512 contiguous bytes, and the loads of two partials are in
+// flight together.  Memory-bound: reads k * 2 KB of partials, writes 1 KB of
+// bf16.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
 #include "mla_internal.h"
+#include "mla_sm103.cuh"
 
 namespace mla {
 namespace {
 
 constexpr int kCombineWarps = 8;
+constexpr int kCombineUnroll = 2;  // partials whose loads are in flight together
 
 __global__ void __launch_bounds__(kCombineWarps * 32)
 combine_kernel(const float *__restrict__ o_accum, const float *__restrict__ lse_accum,
@@ -33,6 +38,7 @@ combine_kernel(const float *__restrict__ o_accum, const float *__restrict__ lse_
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
     const int b = blockIdx.y;
+    sm103::griddep_wait();  // the split-KV kernel's partials (programmatic launch)
     if (row >= rows) return;
     const int first = num_splits[b];
     const int n = num_splits[b + 1] - first;
@@ -42,8 +48,10 @@ combine_kernel(const float *__restrict__ o_accum, const float *__restrict__ lse_
         return;
     }
 
-    float m = -CUDART_INF_F;
-    for (int s = lane; s < n; s += 32) m = fmaxf(m, lse_accum[(size_t)(first + s) * rows + row]);
+    // lane s keeps L_s of partial s (partials past 32 are read again below)
+    const float l_own = lane < n ? lse_accum[(size_t)(first + lane) * rows + row] : -CUDART_INF_F;
+    float m = l_own;
+    for (int s = lane + 32; s < n; s += 32) m = fmaxf(m, lse_accum[(size_t)(first + s) * rows + row]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
 
@@ -53,23 +61,34 @@ combine_kernel(const float *__restrict__ o_accum, const float *__restrict__ lse_
     for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     float total_lse = -CUDART_INF_F;
     if (m != -CUDART_INF_F) {
-        float sum = 0.f;
-        for (int s = lane; s < n; s += 32) sum += __expf(lse_accum[(size_t)(first + s) * rows + row] - m);
+        float sum = lane < n ? __expf(l_own - m) : 0.f;
+        for (int s = lane + 32; s < n; s += 32) sum += __expf(lse_accum[(size_t)(first + s) * rows + row] - m);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
         total_lse = m + __logf(sum);
-        for (int s = 0; s < n; ++s) {
-            const size_t slot = (size_t)(first + s) * rows + row;
-            const float w = __expf(lse_accum[slot] - total_lse);
-            const float4 *src = reinterpret_cast<const float4 *>(o_accum + slot * kDv);
+        const float w_own = lane < n ? __expf(l_own - total_lse) : 0.f;
+        for (int s0 = 0; s0 < n; s0 += kCombineUnroll) {
+            float w[kCombineUnroll];
+            float4 v[kCombineUnroll][4];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float4 v = src[lane + 32 * k];
-                acc[k].x += w * v.x;
-                acc[k].y += w * v.y;
-                acc[k].z += w * v.z;
-                acc[k].w += w * v.w;
+            for (int u = 0; u < kCombineUnroll; ++u) {
+                const int s = s0 + u;  // uniform across the warp
+                const size_t slot = (size_t)(first + (s < n ? s : 0)) * rows + row;
+                w[u] = s < 32 ? __shfl_sync(0xffffffffu, w_own, s & 31) : __expf(lse_accum[slot] - total_lse);
+                if (s >= n) w[u] = 0.f;
+                const float4 *src = reinterpret_cast<const float4 *>(o_accum + slot * kDv);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) v[u][k] = s < n ? src[lane + 32 * k] : make_float4(0.f, 0.f, 0.f, 0.f);
             }
+#pragma unroll
+            for (int u = 0; u < kCombineUnroll; ++u)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    acc[k].x += w[u] * v[u][k].x;
+                    acc[k].y += w[u] * v[u][k].y;
+                    acc[k].z += w[u] * v[u][k].z;
+                    acc[k].w += w[u] * v[u][k].w;
+                }
         }
     }
     uint2 *dst = reinterpret_cast<uint2 *>(o + out_row * kDv);
@@ -88,10 +107,17 @@ combine_kernel(const float *__restrict__ o_accum, const float *__restrict__ lse_
 }  // namespace
 
 cudaError_t launch_combine(const DecodeParams &p, cudaStream_t stream) {
-    dim3 grid((p.rows + kCombineWarps - 1) / kCombineWarps, p.batch);
-    combine_kernel<<<grid, kCombineWarps * 32, 0, stream>>>(p.o_accum, p.lse_accum, p.num_splits, p.rows,
-                                                           p.max_splits, p.o, p.lse, p.status);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((p.rows + kCombineWarps - 1) / kCombineWarps, p.batch, 1);
+    cfg.blockDim = dim3(kCombineWarps * 32, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;  // launch overlaps the split kernel's tail
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, combine_kernel, (const float *)p.o_accum, (const float *)p.lse_accum,
+                              (const int32_t *)p.num_splits, p.rows, p.max_splits, p.o, p.lse, p.status);
 }
 
 }  // namespace mla

@@ -301,5 +301,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 __device__ __forceinline__ bool elect_one_lane() { return (threadIdx.x & 31) == 0; }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// Wait until the grids this one depends on have completed and their writes
+// are visible (returns at once when the launch was not programmatic).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the grids that depend on this one be scheduled (they still wait for its
+// completion before touching its results).
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 }  // namespace sm103
 }  // namespace mla

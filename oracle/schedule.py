@@ -9,16 +9,20 @@ name the two outputs but not how they are built; this is the partition that
 this library defines for them, written out step by step so that the CUDA
 scheduler's output can be compared with it bit for bit:
 
-  1. n_b   = ceil(cache_seqlens[b] / page)            pages of sequence b
-  2. cost  = sum_b (n_b + F)                           F = fixed cost of a segment
-  3. quota = ceil(cost / num_parts) + F   (so every part can take a page)
-  4. Walk the sequences in order with a cursor (b, page).  Part p starts at the
-     cursor with budget ``quota`` (the last part: unbounded).  While sequences
-     remain: if the rest of sequence b plus F fits in the budget, the part
-     finishes b (the cursor moves to (b+1, 0)); otherwise, when budget - F > 0,
-     it takes budget - F more pages of b and stops, else it stops.
-  5. Part p covers the cursor range [begin, end).  ``num_splits`` is the prefix
-     sum over sequences of the number of parts that touch each sequence.
+  1. n_b = ceil(cache_seqlens[b] / page)                pages of sequence b
+  2. Lay the sequences on one line of cost units: sequence b takes c_b = F + n_b
+     units (F = fixed cost of a segment, then one unit per page), starting at
+     S_b = c_0 + ... + c_{b-1}; total = S_batch.
+  3. Q = ceil(total / num_parts).  Part p starts at unit x_p = p * Q (the last
+     part ends at ``total``).
+  4. A unit x maps to a cursor (b, page): b is the sequence whose units hold x
+     (S_b <= x < S_{b+1}); if x lies in its first F units the cursor is
+     (b, 0), otherwise (b, x - S_b - F); x >= total maps to (batch, 0).
+  5. Part p covers the cursor range [cursor(x_p), cursor(x_{p+1})).  A part
+     that starts inside a sequence's pages pays F more than its units, so
+     every part costs at most Q + F pages-equivalent.
+  6. ``num_splits`` is the prefix sum over sequences of the number of parts
+     that touch each sequence.
 
 Metadata row of a part (int32 x 8):
   [begin_b, begin_page, end_b, end_page, begin_split, 0, 0, 0]
@@ -42,27 +46,33 @@ def schedule(cache_seqlens, num_parts: int, page: int = 64, fixed_cost: int = SC
         raise ValueError("negative sequence length")
     batch = len(seqlens)
     n_pages = [(s + page - 1) // page for s in seqlens]
-    total = sum(n + fixed_cost for n in n_pages)
-    quota = (total + num_parts - 1) // num_parts + fixed_cost
+    starts = [0]                                  # S_b
+    for n in n_pages:
+        starts.append(starts[-1] + fixed_cost + n)
+    total = starts[-1]
+    quota = -(-total // num_parts)
 
+    def cursor(x):
+        if x >= total:
+            return batch, 0
+        b = 0
+        while starts[b + 1] <= x:
+            b += 1
+        offset = x - starts[b]
+        return (b, 0) if offset <= fixed_cost else (b, offset - fixed_cost)
+
+    bounds = [cursor(p * quota) for p in range(num_parts)] + [(batch, 0)]
     metadata = np.zeros((num_parts, METADATA_INTS), dtype=np.int32)
-    num_splits = np.zeros(batch + 1, dtype=np.int32)
-    b, pg, parts_on_b = 0, 0, 0
+    touching = [0] * batch                        # parts touching each sequence, so far
     for p in range(num_parts):
-        begin_b, begin_page, begin_split = b, pg, parts_on_b
-        last = p == num_parts - 1
-        budget = quota
-        while b < batch:
-            remaining = n_pages[b] - pg
-            if last or remaining + fixed_cost <= budget:
-                budget -= remaining + fixed_cost
-                num_splits[b + 1] = num_splits[b] + parts_on_b + 1
-                b, pg, parts_on_b = b + 1, 0, 0
-            else:
-                take = budget - fixed_cost
-                if take > 0:
-                    pg += take
-                    parts_on_b += 1
-                break
-        metadata[p, :5] = (begin_b, begin_page, b, pg, begin_split)
+        (b0, pg0), (b1, pg1) = bounds[p], bounds[p + 1]
+        metadata[p, :5] = (b0, pg0, b1, pg1, touching[b0] if b0 < batch else 0)
+        if (b0, pg0) == (b1, pg1):
+            continue
+        last = b1 if pg1 > 0 else b1 - 1          # last sequence this part reaches
+        for b in range(b0, last + 1):
+            touching[b] += 1
+    num_splits = np.zeros(batch + 1, dtype=np.int32)
+    for b in range(batch):
+        num_splits[b + 1] = num_splits[b] + touching[b]
     return metadata, num_splits

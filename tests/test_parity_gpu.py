@@ -121,6 +121,20 @@ def test_scheduler_matches_oracle_partition():
         assert np.array_equal(ns.cpu().numpy(), ns_ref), trial
 
 
+@pytest.mark.parametrize("batch,parts", [(9000, 152), (300, 600), (8191, 256), (8192, 257), (1, 1), (5, 1000)])
+def test_scheduler_large_batches_and_part_counts(batch, parts):
+    # past the scheduler's shared-memory staging (8192 sequences, 256 parts)
+    # the overflow goes straight to global memory; the partition must not change
+    import mla_decode_attention_latent_gb300 as mla
+    rng = np.random.default_rng(batch + parts)
+    sl = rng.integers(0, 5000, size=batch).astype(np.int32)
+    sl[rng.random(batch) < 0.1] = 0
+    md, ns = mla.mla_get_metadata(torch.from_numpy(sl).to(DEV), 128, 1, num_parts=parts)
+    md_ref, ns_ref = oracle.schedule(sl, parts)
+    assert np.array_equal(md.cpu().numpy(), md_ref)
+    assert np.array_equal(ns.cpu().numpy(), ns_ref)
+
+
 def test_deterministic():
     c = case("det", 2, 1, 128, [2000, 900], seed=110)
     x = to_device(W.make_inputs(c, "cpu"), DEV)

@@ -82,13 +82,28 @@ def test_named_partitions(seqlens, num_parts):
 
 
 def test_hand_worked_example():
-    # seqlens {100, 37}: 2 and 1 pages; F = 5; cost = 13; 76 parts -> quota = 1 + 5 = 6.
-    # part 0: sequence 0 needs 2 + 5 > 6, so it takes 6 - 5 = 1 page -> cursor (0, 1)
-    # part 1: the rest of sequence 0 costs 1 + 5 = 6 <= 6 -> finishes it; budget 0
-    # part 2: sequence 1 costs 1 + 5 = 6 <= 6 -> finishes it; later parts are empty
+    # seqlens {100, 37}: 2 and 1 pages; F = 5.  Units: sequence 0 holds
+    # [0, 7) (F = [0, 5), pages at 5 and 6), sequence 1 holds [7, 13)
+    # (F = [7, 12), its page at 12); total 13, 76 parts -> Q = 1, x_p = p.
+    # cursor(0..5) = (0, 0), cursor(6) = (0, 1), cursor(7..12) = (1, 0),
+    # cursor(13..) = (2, 0).  So part 5 = [(0,0), (0,1)), part 6 = [(0,1), (1,0))
+    # (the second piece of sequence 0), part 12 = [(1,0), (2,0)); all others empty.
     md, ns = schedule([100, 37], 76)
-    assert md[0, :5].tolist() == [0, 0, 0, 1, 0]
-    assert md[1, :5].tolist() == [0, 1, 1, 0, 1]
-    assert md[2, :5].tolist() == [1, 0, 2, 0, 0]
-    assert all(md[p, :5].tolist() == [2, 0, 2, 0, 0] for p in range(3, 76))
+    assert md[5, :5].tolist() == [0, 0, 0, 1, 0]
+    assert md[6, :5].tolist() == [0, 1, 1, 0, 1]
+    assert md[12, :5].tolist() == [1, 0, 2, 0, 0]
+    assert all(md[p, :5].tolist() == [0, 0, 0, 0, 0] for p in range(0, 5))
+    assert all(md[p, :5].tolist() == [1, 0, 1, 0, 0] for p in range(7, 12))
+    assert all(md[p, :5].tolist() == [2, 0, 2, 0, 0] for p in range(13, 76))
     assert ns.tolist() == [0, 2, 3]
+
+
+def test_uniform_parts_fill_the_grid():
+    # 64 sequences of 64 pages, 76 parts: units per sequence 69, total 4416,
+    # Q = 59.  Part 0 = units [0, 59) = sequence 0 pages [0, 54); part 1 starts
+    # at unit 59 = (0, 54) and ends at unit 118 = sequence 1 offset 49 = page 44.
+    md, ns = schedule([4096] * 64, 76)
+    assert md[0, :5].tolist() == [0, 0, 0, 54, 0]
+    assert md[1, :5].tolist() == [0, 54, 1, 44, 1]
+    assert int(ns[-1]) == sum(1 + sum(1 for q in range(1, 76) if 69 * b + 5 < 59 * q < 69 * (b + 1))
+                              for b in range(64))
