@@ -526,39 +526,40 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
             const bool raw = nvalid == kPage && sc > 0.f;
             const float fsc = raw ? sc : 1.f;
             float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
-            if (raw) {
+            if (!raw) {
 #pragma unroll
-                for (int j = 0; j < 64; ++j) mx4[j & 3] = fmaxf(mx4[j & 3], __uint_as_float(sr[j]));
-            } else {
-#pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    const float xs = (j < nvalid) ? __uint_as_float(sr[j]) * sc : -CUDART_INF_F;
-                    sr[j] = __float_as_uint(xs);
-                    mx4[j & 3] = fmaxf(mx4[j & 3], xs);
-                }
+                for (int j = 0; j < 64; ++j)
+                    sr[j] = __float_as_uint((j < nvalid) ? __uint_as_float(sr[j]) * sc : -CUDART_INF_F);
             }
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                mx4[j & 3] = max3f(mx4[j & 3], __uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1]));
             const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * fsc;
             float fac = 1.f;
             if (mx > m + kRescaleLog2 || (m == -CUDART_INF_F && mx > -CUDART_INF_F)) {
                 fac = ex2(m - mx);  // 0 when m was -inf
                 m = mx;
             }
-            float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+            // exponent inputs and the row sum two lanes per instruction
+            uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
             uint32_t pk[32];
             if (m == -CUDART_INF_F) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) pk[j] = 0u;
             } else {
-                const float nm = -m;
+                const uint64_t sc2 = f2_pack(fsc, fsc), nm2 = f2_pack(-m, -m);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    const float a = ex2(fmaf(__uint_as_float(sr[2 * j]), fsc, nm));
-                    const float b = ex2(fmaf(__uint_as_float(sr[2 * j + 1]), fsc, nm));
-                    sum4[j & 3] += a + b;
+                    float xa, xb;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1])), sc2, nm2), xa, xb);
+                    const float a = ex2(xa), b = ex2(xb);
+                    sum2[j & 3] = f2_add(sum2[j & 3], f2_pack(a, b));
                     pk[j] = pack_bf16(a, b);
                 }
             }
-            const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+            float sum_lo, sum_hi;
+            f2_unpack(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), sum_lo, sum_hi);
+            const float sum = sum_lo + sum_hi;
             l = l * fac + sum;
 
             // staging pb is free once the value CTA's MMA of page it - 2 is
