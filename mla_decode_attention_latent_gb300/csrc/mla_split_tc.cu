@@ -111,9 +111,8 @@ enum Bar {
     // value CTA
     B_VFULL = B_PFREE + kPBufs, B_VEMPTY = B_VFULL + kVStages, B_PFULL = B_VEMPTY + kVStages,
     B_PREADY = B_PFULL + kPBufs, B_PVDONE = B_PREADY + kPBufs, B_ODONE = B_PVDONE + 1, B_OEMPTY = B_ODONE + 1,
-    B_EPI = B_OEMPTY + 1,
     // both
-    B_FINAL = B_EPI + 1, B_COUNT = B_FINAL + 1
+    B_FINAL = B_OEMPTY + 1, B_COUNT = B_FINAL + 1
 };
 constexpr uint32_t kTmemSlotOff = kBarOff + B_COUNT * 8;
 constexpr uint32_t kAbortOff = kTmemSlotOff + 4;
@@ -192,16 +191,6 @@ __device__ __forceinline__ bool wait(const Ctx &c, int bar_idx, uint32_t parity)
 template <bool kCluster = false>
 __device__ __forceinline__ bool warp_wait(const Ctx &c, int bar_idx, uint32_t parity) {
     return __all_sync(0xffffffffu, wait<kCluster>(c, bar_idx, parity));
-}
-
-// barrier among the 128 row threads built on an mbarrier, so that it is
-// bounded like every other wait (a plain bar.sync would hang if a peer warp
-// had given up on a timeout)
-__device__ __forceinline__ bool group_sync(const Ctx &c, int bar_idx, uint32_t &phase) {
-    mbar_arrive(c.bar(bar_idx));
-    const bool ok = warp_wait(c, bar_idx, phase & 1);
-    ++phase;
-    return ok;
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -566,11 +555,12 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
             // done: that MMA consumed the bulk copy made from it
             if (!warp_wait<true>(c, B_PFREE + pb, ((it / kPBufs) & 1) ^ 1)) return;
             uint8_t *stage = c.base + kStageOff + pb * kPMsgBytes;
-            uint4 *prow = reinterpret_cast<uint4 *>(stage + r * 128);
+            const uint32_t stage_s = smem_u32(stage);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) prow[j ^ (r & 7)] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-            reinterpret_cast<float *>(stage + kFacOff)[r] = fac;
-            if (pg == s.p1 - 1) reinterpret_cast<float *>(stage + kInvLOff)[r] = l > 0.f ? 1.f / l : 0.f;
+            for (int j = 0; j < 8; ++j)
+                sts128(stage_s + r * 128 + 16 * (j ^ (r & 7)), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            sts32(stage_s + kFacOff + 4 * r, __float_as_uint(fac));
+            if (pg == s.p1 - 1) sts32(stage_s + kInvLOff + 4 * r, __float_as_uint(l > 0.f ? 1.f / l : 0.f));
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -610,8 +600,7 @@ __device__ void value_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
     const int r = 32 * (warp & 3) + lane;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const int tid = threadIdx.x - 64;  // 0..127 among the row warps
-    uint8_t *epi = c.base + kEpiOff;
-    uint32_t epi_phase = 0;
+    const uint32_t epi_s = smem_u32(c.base + kEpiOff);
     PartWalk walk;
     walk.init(p, part);
     Segment s;
@@ -621,9 +610,9 @@ __device__ void value_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
         for (int pg = s.p0; pg < s.p1; ++pg, ++it) {
             const int pb = it % kPBufs, st = it % kVStages;
             if (!warp_wait<true>(c, B_PFULL + pb, (it / kPBufs) & 1)) return;
-            const uint8_t *buf = c.base + kPBufOff + pb * kPMsgBytes;
-            const float fac = reinterpret_cast<const float *>(buf + kFacOff)[r];
-            if (pg == s.p1 - 1) inv_l = reinterpret_cast<const float *>(buf + kInvLOff)[r];
+            const uint32_t buf_s = smem_u32(c.base + kPBufOff + pb * kPMsgBytes);
+            const float fac = __uint_as_float(lds32(buf_s + kFacOff + 4 * r));
+            if (pg == s.p1 - 1) inv_l = __uint_as_float(lds32(buf_s + kInvLOff + 4 * r));
             // rows past the sequence's end in its last page: zero them in V so
             // that garbage (even NaN) times a zero weight stays zero
             const int tail = s.T - pg * kPage;
@@ -660,7 +649,7 @@ __device__ void value_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
         }
         // epilogue: O / l -> bf16 output, or fp32 partial for the combine.
         // Each 64-column chunk goes TMEM -> registers -> smem (row per
-        // thread), then every warp writes 32 whole rows with coalesced stores.
+        // thread), then the warp writes its 32 whole rows with coalesced stores.
         const bool has_pages = s.p1 > s.p0;
         if (has_pages) {
             // every P V of the segment has landed.  (The per-page barrier
@@ -680,7 +669,9 @@ __device__ void value_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
                 slot = -1;
             }
         }
-        const int wrow0 = 32 * (tid >> 5);  // rows this warp writes out
+        // each warp stores the 32 rows of its own TMEM lane quarter, through
+        // its own slice of the staging tile: no cross-warp barrier is needed
+        const int wrow0 = 32 * (warp & 3);
 #pragma unroll 1
         for (int ch = 0; ch < kDv / (int)kEpiCols; ++ch) {
             uint32_t v[64];
@@ -690,53 +681,64 @@ __device__ void value_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
                 tmem_ld32(tmem + lane_base + ch * kEpiCols, lo);
                 tmem_ld32(tmem + lane_base + ch * kEpiCols + 32, hi);
                 tmem_wait_ld();
+                if (ch == kDv / (int)kEpiCols - 1) {  // the last TMEM read: O may be overwritten now
+                    tc_fence_before();
+                    mbar_arrive(c.bar(B_OEMPTY));
+                }
             } else {
 #pragma unroll
                 for (int j = 0; j < 64; ++j) v[j] = 0u;
             }
-            float4 *srow = reinterpret_cast<float4 *>(epi + r * kEpiStride);
+            const uint32_t srow = epi_s + r * kEpiStride;
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-                srow[j] = make_float4(__uint_as_float(v[4 * j]) * inv_l, __uint_as_float(v[4 * j + 1]) * inv_l,
-                                      __uint_as_float(v[4 * j + 2]) * inv_l, __uint_as_float(v[4 * j + 3]) * inv_l);
-            if (!group_sync(c, B_EPI, epi_phase)) return;
+                sts128(srow + 16 * j, __float_as_uint(__uint_as_float(v[4 * j]) * inv_l),
+                       __float_as_uint(__uint_as_float(v[4 * j + 1]) * inv_l),
+                       __float_as_uint(__uint_as_float(v[4 * j + 2]) * inv_l),
+                       __float_as_uint(__uint_as_float(v[4 * j + 3]) * inv_l));
+            __syncwarp();
             if (slot >= 0) {
+                // all of the warp's shared loads first, then its global stores
+                uint4 x[16];
                 if (split) {
                     // fp32: 256 B per row chunk, two rows per warp store
-#pragma unroll 4
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        x[k] = lds128(epi_s + (wrow0 + 2 * k + (lane >> 4)) * kEpiStride + 16 * (lane & 15));
+#pragma unroll
                     for (int k = 0; k < 16; ++k) {
-                        const int row = wrow0 + 2 * k + (lane >> 4);
-                        const int g = tile * kTileRows + row;
-                        const float4 val = reinterpret_cast<const float4 *>(epi + row * kEpiStride)[lane & 15];
+                        const int g = tile * kTileRows + wrow0 + 2 * k + (lane >> 4);
                         if (g < p.rows)
-                            reinterpret_cast<float4 *>(p.o_accum + ((size_t)slot * p.rows + g) * kDv + ch * kEpiCols)[lane & 15] = val;
+                            reinterpret_cast<uint4 *>(p.o_accum + ((size_t)slot * p.rows + g) * kDv + ch * kEpiCols)[lane & 15] = x[k];
                     }
                 } else {
                     // bf16: 128 B per row chunk, four rows per warp store
-#pragma unroll 4
+#pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        const int row = wrow0 + 4 * k + (lane >> 3);
-                        const int g = tile * kTileRows + row;
-                        const float4 *src = reinterpret_cast<const float4 *>(epi + row * kEpiStride) + 2 * (lane & 7);
-                        const float4 a = src[0], b = src[1];
+                        const uint32_t src = epi_s + (wrow0 + 4 * k + (lane >> 3)) * kEpiStride + 32 * (lane & 7);
+                        x[2 * k] = lds128(src);
+                        x[2 * k + 1] = lds128(src + 16);
+                    }
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int g = tile * kTileRows + wrow0 + 4 * k + (lane >> 3);
+                        const uint4 a = x[2 * k], b = x[2 * k + 1];
                         uint4 w;
-                        w.x = pack_bf16(a.x, a.y);
-                        w.y = pack_bf16(a.z, a.w);
-                        w.z = pack_bf16(b.x, b.y);
-                        w.w = pack_bf16(b.z, b.w);
+                        w.x = pack_bf16(__uint_as_float(a.x), __uint_as_float(a.y));
+                        w.y = pack_bf16(__uint_as_float(a.z), __uint_as_float(a.w));
+                        w.z = pack_bf16(__uint_as_float(b.x), __uint_as_float(b.y));
+                        w.w = pack_bf16(__uint_as_float(b.z), __uint_as_float(b.w));
                         if (g < p.rows)
                             reinterpret_cast<uint4 *>(p.o + ((size_t)s.b * p.rows + g) * kDv + ch * kEpiCols)[lane & 7] = w;
                     }
                 }
             }
-            if (!group_sync(c, B_EPI, epi_phase)) return;
-        }
-        if (has_pages) {
-            tc_fence_before();
-            mbar_arrive(c.bar(B_OEMPTY));
+            __syncwarp();  // the slice is rewritten by the next chunk
         }
     }
 }
+
+
 
 
 // -------------------------------------------------------------- kernel
@@ -781,7 +783,6 @@ split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParam
         mbar_init(c.bar(B_PVDONE), 1);
         mbar_init(c.bar(B_ODONE), 1);
         mbar_init(c.bar(B_OEMPTY), 128);
-        mbar_init(c.bar(B_EPI), 128);
         mbar_init(c.bar(B_FINAL), is_score ? kScoreIssuers : 1);  // one commit per MMA issuer
         *c.abort_flag = 0;
         fence_mbar_init();
