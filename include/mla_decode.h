@@ -72,7 +72,9 @@ struct CUstream_st;
 #define MLA_V_DIM 512
 #define MLA_METADATA_INTS 8
 /* fixed cost of one split-KV segment, in pages, used by the work partition */
-#define MLA_SCHED_FIXED_COST_PAGES 5
+#define MLA_SCHED_FIXED_COST_PAGES 8
+/* cost, in pages, that the partition charges for needing the combine pass */
+#define MLA_SCHED_COMBINE_COST_PAGES 4
 
 /* device-side error bits reported through mla_device_status() */
 #define MLA_DEVERR_TIMEOUT 0x1     /* a bounded wait inside a kernel gave up */
@@ -100,7 +102,11 @@ MLA_API int mla_num_sm_parts(int device, int num_q_rows, int h_kv, int *num_part
  * Launches the tile-scheduler kernel on `stream`.  It reads the sequence
  * lengths and cuts the (sequence, page) range into `num_parts` contiguous
  * parts of near-equal cost (pages plus MLA_SCHED_FIXED_COST_PAGES per
- * segment); a sequence may be cut across several parts (split-KV).
+ * segment); a sequence may be cut across several parts (split-KV).  When
+ * the batch is smaller than num_parts and one part per sequence is
+ * estimated to finish sooner (no sequence cut, so no combine, charged
+ * MLA_SCHED_COMBINE_COST_PAGES), only `batch` parts get work and the
+ * others are empty.
  *   cache_seqlens            device int32 [batch]; entries >= 0
  *   batch                    number of sequences (>= 1)
  *   num_q_rows, h_kv         as for mla_num_sm_parts

@@ -15,6 +15,7 @@ constexpr int kDqk = MLA_HEAD_DIM;         // 512 latent + 64 RoPE dims
 constexpr int kDv = MLA_V_DIM;             // value dims = first 512 dims of a row
 constexpr int kMdInts = MLA_METADATA_INTS;
 constexpr int kFixedCost = MLA_SCHED_FIXED_COST_PAGES;
+constexpr int kCombineCost = MLA_SCHED_COMBINE_COST_PAGES;
 
 // Everything a split-KV kernel needs for one decode call.
 struct DecodeParams {

@@ -83,8 +83,31 @@ schedule_kernel(const int32_t *__restrict__ seqlens, int batch, int num_parts,
     const long long first_unit = block_exclusive_scan(cost, s_warp64, &total);
     s_start[threadIdx.x] = first_unit;
     if (threadIdx.x == 0) s_start[kSchedThreads] = total;
-    __syncthreads();
-    const long long quota = (total + num_parts - 1) / num_parts;  // total >= batch * F > 0
+
+    // how many parts get work: all of them, or one per sequence when the
+    // batch is smaller and that is estimated to finish sooner.  A candidate
+    // with quota q costs q, plus F + C when a part would start strictly
+    // inside some sequence's pages (a multiple of q in (S_b + F, S_{b+1})).
+    const long long q_all = (total + num_parts - 1) / num_parts;  // total >= batch * F > 0
+    const long long q_seq = (total + batch - 1) / batch;
+    bool cut_all = false, cut_seq = false;
+    if (batch < num_parts) {
+        long long u = first_unit;
+        for (int i = i0; i < i1; ++i) {
+            const int n = pages_of(seqlens[i]);
+            const long long next = u + n + kFixedCost;
+            if (n > 0) {
+                cut_all |= (next - 1) / q_all > (u + kFixedCost) / q_all;
+                cut_seq |= (next - 1) / q_seq > (u + kFixedCost) / q_seq;
+            }
+            u = next;
+        }
+    }
+    cut_all = __syncthreads_or(cut_all);
+    cut_seq = __syncthreads_or(cut_seq);
+    const long long est_all = q_all + (cut_all ? kFixedCost + kCombineCost : 0);
+    const long long est_seq = q_seq + (cut_seq ? kFixedCost + kCombineCost : 0);
+    const long long quota = (batch < num_parts && est_seq < est_all) ? q_seq : q_all;
 
     // cursor of unit x: sequence b, page, and S_b
     auto cursor = [&](long long x, int &b, int &pg, long long &sb) {

@@ -26,7 +26,7 @@ import threading
 
 import numpy as np
 
-from .schedule import schedule, SCHED_FIXED_COST_PAGES  # noqa: F401
+from .schedule import schedule, SCHED_FIXED_COST_PAGES, SCHED_COMBINE_COST_PAGES  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "mla_oracle.c")

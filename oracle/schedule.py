@@ -13,8 +13,14 @@ scheduler's output can be compared with it bit for bit:
   2. Lay the sequences on one line of cost units: sequence b takes c_b = F + n_b
      units (F = fixed cost of a segment, then one unit per page), starting at
      S_b = c_0 + ... + c_{b-1}; total = S_batch.
-  3. Q = ceil(total / num_parts).  Part p starts at unit x_p = p * Q (the last
-     part ends at ``total``).
+  3. Q = ceil(total / P) with P the number of parts that do work, chosen
+     from two candidates: all ``num_parts``, and (when the batch is smaller)
+     one part per sequence.  A candidate's estimated makespan is Q, plus
+     F + C (C = the combine's cost) when any part start x = p * Q falls
+     strictly inside a sequence's pages; the batch-sized candidate is taken
+     only when its estimate is strictly smaller.  Part p starts at unit
+     x_p = p * Q (the last part ends at ``total``; parts with x_p >= total
+     are empty).
   4. A unit x maps to a cursor (b, page): b is the sequence whose units hold x
      (S_b <= x < S_{b+1}); if x lies in its first F units the cursor is
      (b, 0), otherwise (b, x - S_b - F); x >= total maps to (batch, 0).
@@ -33,11 +39,13 @@ from __future__ import annotations
 
 import numpy as np
 
-SCHED_FIXED_COST_PAGES = 5
+SCHED_FIXED_COST_PAGES = 8
+SCHED_COMBINE_COST_PAGES = 4
 METADATA_INTS = 8
 
 
-def schedule(cache_seqlens, num_parts: int, page: int = 64, fixed_cost: int = SCHED_FIXED_COST_PAGES):
+def schedule(cache_seqlens, num_parts: int, page: int = 64, fixed_cost: int = SCHED_FIXED_COST_PAGES,
+             combine_cost: int = SCHED_COMBINE_COST_PAGES):
     """Return (metadata int32 [num_parts, 8], num_splits int32 [b + 1])."""
     seqlens = [int(x) for x in np.asarray(cache_seqlens).reshape(-1)]
     if num_parts < 1:
@@ -50,7 +58,20 @@ def schedule(cache_seqlens, num_parts: int, page: int = 64, fixed_cost: int = SC
     for n in n_pages:
         starts.append(starts[-1] + fixed_cost + n)
     total = starts[-1]
-    quota = -(-total // num_parts)
+
+    def splits_some_sequence(q):
+        # is any multiple of q strictly inside some sequence's pages?
+        return any(starts[b] + fixed_cost < x < starts[b + 1]
+                   for b in range(batch) for x in range(q * ((starts[b] + fixed_cost) // q + 1), starts[b + 1], q))
+
+    def estimate(parts):
+        q = -(-total // parts)
+        return q + (fixed_cost + combine_cost if splits_some_sequence(q) else 0)
+
+    used = num_parts
+    if batch < num_parts and estimate(batch) < estimate(num_parts):
+        used = batch
+    quota = -(-total // used)
 
     def cursor(x):
         if x >= total:

@@ -47,6 +47,8 @@ def test_fixed_cost_matches_oracle_partition():
     import oracle
     m = re.search(r"#define MLA_SCHED_FIXED_COST_PAGES (\d+)", open(HEADER).read())
     assert int(m.group(1)) == oracle.SCHED_FIXED_COST_PAGES
+    m = re.search(r"#define MLA_SCHED_COMBINE_COST_PAGES (\d+)", open(HEADER).read())
+    assert int(m.group(1)) == oracle.SCHED_COMBINE_COST_PAGES
 
 
 def test_status_strings(lib):

@@ -6,7 +6,7 @@ partition must satisfy plus one example worked by hand.
 import numpy as np
 import pytest
 
-from oracle import schedule, SCHED_FIXED_COST_PAGES
+from oracle import schedule, SCHED_FIXED_COST_PAGES, SCHED_COMBINE_COST_PAGES
 
 PAGE = 64
 
@@ -42,7 +42,9 @@ def check_invariants(seqlens, num_parts, md, ns, fixed=SCHED_FIXED_COST_PAGES):
     assert cursor == (batch, 0), "the last part must end after the last sequence"
     pieces = parts_touching(md, n_pages)
     total = sum(n + fixed for n in n_pages)
-    quota = -(-total // num_parts) + fixed
+    working = sum(1 for row in md if (int(row[0]), int(row[1])) != (int(row[2]), int(row[3])))
+    # the quota the partition used is at most ceil(total / parts with work)
+    quota = -(-total // max(1, working)) + fixed
     for b in range(batch):
         ps = pieces[b]
         assert len(ps) >= 1, "every sequence is touched by at least one part"
@@ -57,8 +59,8 @@ def check_invariants(seqlens, num_parts, md, ns, fixed=SCHED_FIXED_COST_PAGES):
         for k, (p, a, _) in enumerate(ps):
             if int(md[p, 0]) == b:
                 assert int(md[p, 4]) == k
-    # every part but the last keeps within its quota
-    for p, row in enumerate(md[:-1]):
+    # every part keeps within its quota
+    for p, row in enumerate(md):
         cost = sum(e - a + fixed for b in range(batch) for (pp, a, e) in pieces[b] if pp == p)
         assert cost <= quota
 
@@ -82,28 +84,38 @@ def test_named_partitions(seqlens, num_parts):
 
 
 def test_hand_worked_example():
-    # seqlens {100, 37}: 2 and 1 pages; F = 5.  Units: sequence 0 holds
-    # [0, 7) (F = [0, 5), pages at 5 and 6), sequence 1 holds [7, 13)
-    # (F = [7, 12), its page at 12); total 13, 76 parts -> Q = 1, x_p = p.
-    # cursor(0..5) = (0, 0), cursor(6) = (0, 1), cursor(7..12) = (1, 0),
-    # cursor(13..) = (2, 0).  So part 5 = [(0,0), (0,1)), part 6 = [(0,1), (1,0))
-    # (the second piece of sequence 0), part 12 = [(1,0), (2,0)); all others empty.
+    # seqlens {100, 37}: 2 and 1 pages; F = 8.  Units: sequence 0 holds
+    # [0, 10) (its pages at 8 and 9), sequence 1 holds [10, 19) (its page at
+    # 18); total 19.  All 76 parts: Q = 1 and unit 9 is inside sequence 0's
+    # pages, so the estimate is 1 + F + C = 13.  One part per sequence:
+    # Q = 10, and no multiple of 10 is strictly inside a sequence's pages,
+    # estimate 10 < 13: two parts get work.  cursor(0) = (0, 0),
+    # cursor(10) = (1, 0), cursor(20) = (2, 0).
+    assert SCHED_FIXED_COST_PAGES == 8 and SCHED_COMBINE_COST_PAGES == 4
     md, ns = schedule([100, 37], 76)
-    assert md[5, :5].tolist() == [0, 0, 0, 1, 0]
-    assert md[6, :5].tolist() == [0, 1, 1, 0, 1]
-    assert md[12, :5].tolist() == [1, 0, 2, 0, 0]
-    assert all(md[p, :5].tolist() == [0, 0, 0, 0, 0] for p in range(0, 5))
-    assert all(md[p, :5].tolist() == [1, 0, 1, 0, 0] for p in range(7, 12))
-    assert all(md[p, :5].tolist() == [2, 0, 2, 0, 0] for p in range(13, 76))
-    assert ns.tolist() == [0, 2, 3]
+    assert md[0, :5].tolist() == [0, 0, 1, 0, 0]
+    assert md[1, :5].tolist() == [1, 0, 2, 0, 0]
+    assert all(md[p, :5].tolist() == [2, 0, 2, 0, 0] for p in range(2, 76))
+    assert ns.tolist() == [0, 1, 2]
 
 
-def test_uniform_parts_fill_the_grid():
-    # 64 sequences of 64 pages, 76 parts: units per sequence 69, total 4416,
-    # Q = 59.  Part 0 = units [0, 59) = sequence 0 pages [0, 54); part 1 starts
-    # at unit 59 = (0, 54) and ends at unit 118 = sequence 1 offset 49 = page 44.
+def test_uniform_takes_one_part_per_sequence():
+    # 64 sequences of 64 pages, 76 parts: units per sequence 72, total 4608.
+    # All parts: Q = 61, which cuts sequences: estimate 61 + 12 = 73.  One
+    # part per sequence: Q = 72 lands on sequence starts: estimate 72.
     md, ns = schedule([4096] * 64, 76)
-    assert md[0, :5].tolist() == [0, 0, 0, 54, 0]
-    assert md[1, :5].tolist() == [0, 54, 1, 44, 1]
-    assert int(ns[-1]) == sum(1 + sum(1 for q in range(1, 76) if 69 * b + 5 < 59 * q < 69 * (b + 1))
-                              for b in range(64))
+    for p in range(64):
+        assert md[p, :5].tolist() == [p, 0, p + 1, 0, 0]
+    assert all(md[p, :5].tolist() == [64, 0, 64, 0, 0] for p in range(64, 76))
+    assert ns.tolist() == list(range(65))
+
+
+def test_long_sequences_use_every_part():
+    # 64 sequences of 1024 pages, 1032 units each, total 66048: all 76 parts
+    # (Q = 870, estimate 882) beat one part per sequence (Q = 1032); part 0 =
+    # units [0, 870) = sequence 0 pages [0, 862), part 1 starts there and
+    # ends at unit 1740 = sequence 1 offset 708 = page 700.
+    md, ns = schedule([65536] * 64, 76)
+    assert md[0, :5].tolist() == [0, 0, 0, 862, 0]
+    assert md[1, :5].tolist() == [0, 862, 1, 700, 1]
+    assert sum(1 for r in md if (r[0], r[1]) != (r[2], r[3])) == 76
