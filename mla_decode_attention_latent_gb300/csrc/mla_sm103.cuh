@@ -174,6 +174,11 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const vo
 }
 
 // prefetch a contiguous global range into L2
+// bring the line holding `src` into L1 (no register result, never faults)
+__device__ __forceinline__ void prefetch_line_l1(const void *src) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<uint64_t>(src)));
+}
+
 __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
                  : "memory");

@@ -253,6 +253,15 @@ __device__ void score_producer(const DecodeParams &p, const Ctx &c, const CUtens
     PartWalk walk;
     Segment s;
     PagePrefetcher ahead;
+    {
+        // the block-table line of the part's first page travels while the
+        // walk reads the sequence lengths (one dependent round trip fewer
+        // before the first chunk load)
+        const int32_t *md = p.metadata + (size_t)part * kMdInts;
+        const int bb = md[0], bp = md[1];
+        if (bb >= 0 && bb < p.batch && bp >= 0 && bp < p.max_blocks)
+            prefetch_line_l1(p.block_table + (size_t)bb * p.max_blocks + bp);
+    }
     if (r == 0) {
         const int rows = min(kTileRows, p.rows - tile * kTileRows);
         walk.init(p, part);
@@ -690,12 +699,22 @@ __device__ void value_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
                 for (int j = 0; j < 64; ++j) v[j] = 0u;
             }
             const uint32_t srow = epi_s + r * kEpiStride;
+            if (split) {  // fp32 partial: 256 B of the row
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                sts128(srow + 16 * j, __float_as_uint(__uint_as_float(v[4 * j]) * inv_l),
-                       __float_as_uint(__uint_as_float(v[4 * j + 1]) * inv_l),
-                       __float_as_uint(__uint_as_float(v[4 * j + 2]) * inv_l),
-                       __float_as_uint(__uint_as_float(v[4 * j + 3]) * inv_l));
+                for (int j = 0; j < 16; ++j)
+                    sts128(srow + 16 * j, __float_as_uint(__uint_as_float(v[4 * j]) * inv_l),
+                           __float_as_uint(__uint_as_float(v[4 * j + 1]) * inv_l),
+                           __float_as_uint(__uint_as_float(v[4 * j + 2]) * inv_l),
+                           __float_as_uint(__uint_as_float(v[4 * j + 3]) * inv_l));
+            } else {  // bf16 output: 128 B of the row
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    sts128(srow + 16 * j,
+                           pack_bf16(__uint_as_float(v[8 * j]) * inv_l, __uint_as_float(v[8 * j + 1]) * inv_l),
+                           pack_bf16(__uint_as_float(v[8 * j + 2]) * inv_l, __uint_as_float(v[8 * j + 3]) * inv_l),
+                           pack_bf16(__uint_as_float(v[8 * j + 4]) * inv_l, __uint_as_float(v[8 * j + 5]) * inv_l),
+                           pack_bf16(__uint_as_float(v[8 * j + 6]) * inv_l, __uint_as_float(v[8 * j + 7]) * inv_l));
+            }
             __syncwarp();
             if (slot >= 0) {
                 // all of the warp's shared loads first, then its global stores
@@ -714,22 +733,13 @@ __device__ void value_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
                 } else {
                     // bf16: 128 B per row chunk, four rows per warp store
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const uint32_t src = epi_s + (wrow0 + 4 * k + (lane >> 3)) * kEpiStride + 32 * (lane & 7);
-                        x[2 * k] = lds128(src);
-                        x[2 * k + 1] = lds128(src + 16);
-                    }
+                    for (int k = 0; k < 8; ++k)
+                        x[k] = lds128(epi_s + (wrow0 + 4 * k + (lane >> 3)) * kEpiStride + 16 * (lane & 7));
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
                         const int g = tile * kTileRows + wrow0 + 4 * k + (lane >> 3);
-                        const uint4 a = x[2 * k], b = x[2 * k + 1];
-                        uint4 w;
-                        w.x = pack_bf16(__uint_as_float(a.x), __uint_as_float(a.y));
-                        w.y = pack_bf16(__uint_as_float(a.z), __uint_as_float(a.w));
-                        w.z = pack_bf16(__uint_as_float(b.x), __uint_as_float(b.y));
-                        w.w = pack_bf16(__uint_as_float(b.z), __uint_as_float(b.w));
                         if (g < p.rows)
-                            reinterpret_cast<uint4 *>(p.o + ((size_t)s.b * p.rows + g) * kDv + ch * kEpiCols)[lane & 7] = w;
+                            reinterpret_cast<uint4 *>(p.o + ((size_t)s.b * p.rows + g) * kDv + ch * kEpiCols)[lane & 7] = x[k];
                     }
                 }
             }
