@@ -135,6 +135,67 @@ def test_scheduler_large_batches_and_part_counts(batch, parts):
     assert np.array_equal(ns.cpu().numpy(), ns_ref)
 
 
+def test_programmatic_launch_sees_the_previous_kernels_writes():
+    # the split-KV and combine kernels are programmatic dependents of the
+    # kernel before them on the stream: a decode issued right after a kernel
+    # that rewrites q (no host sync, no event between) must read the new q
+    import mla_decode_attention_latent_gb300 as mla
+    c = case("pdl", 3, 2, 64, [300, 1000, 77], causal=True, seed=115)
+    x_cpu = W.make_inputs(c, "cpu")
+    o_ref, lse_ref = oracle_of(x_cpu)
+    x = to_device(x_cpu, DEV)
+    md, ns = mla.mla_get_metadata(x.cache_seqlens, c.num_q_rows, c.h_kv)
+    q_true = x.q.clone()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        x.q.zero_()                  # a decode of this q would give O = mean V
+        x.q.copy_(q_true)            # the kernel right before the decode restores it
+        o, lse = mla.mla_decode_kvcache(x.q, x.kcache, x.block_table, x.cache_seqlens, c.dv, md, ns,
+                                        softmax_scale=c.softmax_scale, causal=c.causal)
+    torch.cuda.synchronize()
+    assert mla.mla_device_status(clear=True) == 0
+    assert_parity(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "programmatic launch")
+
+
+def test_graph_capture_matches_eager():
+    # scheduler + decode captured in a CUDA graph (fixed buffers) and
+    # replayed give the eager results bit for bit
+    import mla_decode_attention_latent_gb300 as mla
+    c = case("graph", 4, 1, 128, [4096, 900, 65, 2000], seed=116)
+    x = to_device(W.make_inputs(c, "cpu"), DEV)
+    parts = mla.mla_num_sm_parts(c.num_q_rows, c.h_kv, DEV)
+    o_e, l_e, *_ = run_gpu(x)
+    md = torch.empty((parts, 8), dtype=torch.int32, device=DEV)
+    ns = torch.empty((c.batch + 1,), dtype=torch.int32, device=DEV)
+    o = torch.empty_like(o_e)
+    lse = torch.empty_like(l_e)
+    ws = torch.empty((mla.mla_workspace_bytes(c.batch, c.s_q, c.h_q, c.h_kv, c.dv, parts),), dtype=torch.uint8,
+                     device=DEV)
+    from mla_decode_attention_latent_gb300 import _lib as lib
+    stream = torch.cuda.Stream()
+
+    def step():
+        st = lib.load().mla_get_metadata(x.cache_seqlens.data_ptr(), c.batch, c.num_q_rows, c.h_kv, parts,
+                                         md.data_ptr(), ns.data_ptr(), stream.cuda_stream)
+        assert st == 0
+        mla.mla_decode_kvcache(x.q, x.kcache, x.block_table, x.cache_seqlens, c.dv, md, ns,
+                               softmax_scale=c.softmax_scale, causal=c.causal, out=o, lse=lse, workspace=ws)
+
+    with torch.cuda.stream(stream):
+        step()                       # first call outside the capture (one-time set-up)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    o.zero_()
+    lse.zero_()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    assert mla.mla_device_status(clear=True) == 0
+    assert torch.equal(o, o_e) and torch.equal(lse, l_e)
+
+
 def test_deterministic():
     c = case("det", 2, 1, 128, [2000, 900], seed=110)
     x = to_device(W.make_inputs(c, "cpu"), DEV)
