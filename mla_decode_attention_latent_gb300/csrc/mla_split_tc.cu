@@ -83,8 +83,6 @@ constexpr uint32_t kSCol0 = kQCols;                        // S buffers follow Q
 constexpr uint32_t kSCols = 2 * kPage;                     // an S buffer holds the scores of two pages
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;                       // lazy rescale threshold (log2 units)
-constexpr uint32_t kScoreAheadPages = 0;                   // pages the score CTA requests into L2 ahead of its loads
-constexpr uint32_t kValueAheadPages = 0;                   // pages the value CTA requests into L2 ahead of its loads
 constexpr uint32_t kEpiCols = 64;                          // epilogue chunk: 64 fp32 columns
 constexpr uint32_t kEpiStride = kEpiCols * 4 + 16;         // padded row stride (conflict-free v4 stores)
 
@@ -209,50 +207,18 @@ __device__ __forceinline__ int safe_block(const DecodeParams &p, int b, int page
 }
 
 // -------------------------------------------------------------- roles
-// Streams the part's pages into L2 ahead of their use: one bulk prefetch of a
-// whole contiguous 72 KB page, issued by the score CTA's producer lane.
-struct PagePrefetcher {
-    PartWalk walk;
-    Segment s;
-    int pg;
-    bool live;
-    uint32_t issued;
-    __device__ void init(const DecodeParams &p, int part) {
-        walk.init(p, part);
-        live = walk.next(p, s);
-        pg = live ? s.p0 : 0;
-        issued = 0;
-    }
-    // issue prefetches until `target` pages of the part have been requested
-    __device__ void run(const DecodeParams &p, uint32_t target) {
-        while (live && issued < target) {
-            if (pg >= s.p1) {
-                live = walk.next(p, s);
-                pg = live ? s.p0 : 0;
-                continue;
-            }
-            const int blk = p.block_table[(size_t)s.b * p.max_blocks + pg];
-            if (blk >= 0 && (int64_t)blk < p.num_blocks)
-                prefetch_l2(p.kcache + (size_t)blk * kPage * kDqk, kPage * kDqk * 2);
-            ++pg;
-            ++issued;
-        }
-    }
-};
-
 // Score-CTA TMA producers (one lane each, one per MMA issuer's ring `r`,
 // taking the steps of parity r).  A step is up to two consecutive pages
 // of a segment; each of a step's 9 64-dim chunks is one 16 KB ring slot
 // holding 128 token rows (first page rows 0-63, second page rows 64-127), so
 // that one tcgen05 MMA with N = 128 covers both pages.  Producer 0 first asks
 // L2 for the Q rows of every segment.  (Streaming whole pages into L2 ahead
-// of the chunk loads, from either CTA, measured slower on GB300 at every
-// distance tried, so both distances are 0.)
+// of the chunk loads, from either CTA and at any distance tried, measured
+// slower on GB300 than letting the chunk loads fetch them.)
 __device__ void score_producer(const DecodeParams &p, const Ctx &c, const CUtensorMap *map, int part, int tile,
                                int r) {
     PartWalk walk;
     Segment s;
-    PagePrefetcher ahead;
     {
         // the block-table line of the part's first page travels while the
         // walk reads the sequence lengths (one dependent round trip fewer
@@ -268,21 +234,15 @@ __device__ void score_producer(const DecodeParams &p, const Ctx &c, const CUtens
         while (walk.next(p, s))
             if (s.p1 > s.p0 && rows > 0)
                 prefetch_l2(p.q + ((size_t)s.b * p.rows + (size_t)tile * kTileRows) * kDqk, (uint32_t)rows * kDqk * 2);
-        if (kScoreAheadPages > 0) {
-            ahead.init(p, part);
-            ahead.run(p, kScoreAheadPages);
-        }
     }
     walk.init(p, part);
     uint32_t ring_it = 0;  // chunks issued into this producer's ring
-    uint32_t step = 0, pages_done = 0;
+    uint32_t step = 0;
     bool ok = true;
     while (ok && walk.next(p, s)) {
         for (int pg = s.p0; ok && pg < s.p1; pg += 2, ++step) {
             const int npg = min(2, s.p1 - pg);
-            pages_done += npg;
             if ((int)(step % kScoreIssuers) != r) continue;  // the other ring's step
-            if (kScoreAheadPages > 0 && r == 0) ahead.run(p, pages_done + kScoreAheadPages);
             const int blk0 = safe_block(p, s.b, pg);
             const int blk1 = npg > 1 ? safe_block(p, s.b, pg + 1) : 0;
             for (int ch = 0; ch < kKChunks; ++ch) {
@@ -309,18 +269,12 @@ __device__ void score_producer(const DecodeParams &p, const Ctx &c, const CUtens
 __device__ void value_producer(const DecodeParams &p, const Ctx &c, const CUtensorMap *map, int part) {
     PartWalk walk;
     Segment s;
-    PagePrefetcher ahead;
-    if (kValueAheadPages > 0) {
-        ahead.init(p, part);
-        ahead.run(p, kValueAheadPages);
-    }
     walk.init(p, part);
     uint32_t it = 0;
     bool ok = true;
     while (ok && walk.next(p, s)) {
         for (int pg = s.p0; pg < s.p1; ++pg, ++it) {
             const int st = it % kVStages;
-            if (kValueAheadPages > 0) ahead.run(p, it + 1 + kValueAheadPages);
             if (!wait(c, B_VEMPTY + st, ((it / kVStages) & 1) ^ 1)) {
                 ok = false;
                 break;
