@@ -36,8 +36,11 @@
  *  - bf16 tensors are raw IEEE bfloat16 bit patterns (2 bytes per element),
  *    row-major and densely packed in the shapes given.
  *
- * Supported on the GPU path: d = 576, dv = 512, page size 64, h_kv = 1,
- * any batch >= 1, any s_q >= 1 and h_q >= 1 with s_q * h_q <= 65536.
+ * Supported on the GPU path: d = 576 or 512, dv = 512, page size 64,
+ * h_kv = 1, any batch >= 1, any s_q >= 1 and h_q >= 1 with
+ * s_q * h_q <= 65536.  d = 512 is the d_qk = 512 variant that the
+ * "[FlashInfer] ... SM120 sparse MLA" page names for DSv4, read as a
+ * 512-dim cached row that is both key and value (no separate RoPE part).
  * Other shapes return MLA_ERR_UNSUPPORTED.
  */
 #ifndef MLA_DECODE_H
@@ -139,7 +142,7 @@ MLA_API size_t mla_workspace_bytes(int batch, int s_q, int h_q, int h_kv, int dv
  * For batch b, query token i, head h (all heads share KV head 0):
  *   T    = cache_seqlens[b]                 (causal == 0, or s_q == 1)
  *   T    = cache_seqlens[b] - s_q + i + 1   (causal != 0)
- *   k_j  = kcache[block_table[b][j / 64]][j % 64][0][0..576),   j < T
+ *   k_j  = kcache[block_table[b][j / 64]][j % 64][0][0..d),     j < T
  *   s_j  = softmax_scale * <q[b][i][h], k_j>
  *   lse  = ln sum_j exp(s_j)
  *   o    = sum_j exp(s_j - lse) * k_j[0..512)
@@ -152,7 +155,7 @@ MLA_API size_t mla_workspace_bytes(int batch, int s_q, int h_q, int h_kv, int dv
  *   block_table    device int32 [batch][max_blocks_per_seq]; the first
  *                  ceil(T_b / 64) entries of row b must lie in [0, num_blocks)
  *   cache_seqlens  device int32 [batch]; 0 <= T_b <= 64 * max_blocks_per_seq
- *   d, dv          576 and 512
+ *   d, dv          576 (or 512) and 512
  *   tile_scheduler_metadata, num_splits, num_parts
  *                  from mla_get_metadata with the same cache_seqlens
  *   softmax_scale  multiplies q.k before the softmax (e.g. 1/sqrt(576))

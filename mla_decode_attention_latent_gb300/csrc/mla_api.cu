@@ -69,7 +69,7 @@ int mla_num_sm_parts(int device, int num_q_rows, int h_kv, int *num_parts) {
     if (device != prev && cudaSetDevice(device) != cudaSuccess) return MLA_ERR_CUDA;
     // one CTA pair (two SMs) per part and row tile: as many pairs as fit at once
     int pairs = 0;
-    cudaError_t e = split_kv_tc_max_pairs(&pairs);
+    cudaError_t e = split_kv_tc_max_pairs<576>(&pairs);  // both row widths fit one CTA per SM
     if (device != prev) cudaSetDevice(prev);
     if (e != cudaSuccess) return MLA_ERR_CUDA;
     if (pairs < 1) pairs = 1;
@@ -111,7 +111,7 @@ int mla_decode_kvcache(const void *q, const void *kcache, int64_t num_blocks, co
         max_blocks_per_seq < 1 || num_parts < 1 || d < 1 || dv < 1)
         return MLA_ERR_INVALID_ARG;
     if (!(softmax_scale == softmax_scale)) return MLA_ERR_INVALID_ARG;
-    if (d != kDqk || dv != kDv || h_kv != 1) return MLA_ERR_UNSUPPORTED;
+    if ((d != kDqk && d != kDv) || dv != kDv || h_kv != 1) return MLA_ERR_UNSUPPORTED;
     if ((long long)s_q * h_q > kMaxRows) return MLA_ERR_UNSUPPORTED;
     if ((long long)max_blocks_per_seq * kPage > 0x7fffffffLL) return MLA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(kcache) || !aligned16(o) || !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
@@ -148,7 +148,7 @@ int mla_decode_kvcache(const void *q, const void *kcache, int64_t num_blocks, co
         ev_end = g_split_end;
     }
     if (ev_begin && cudaEventRecord(ev_begin, s) != cudaSuccess) return MLA_ERR_CUDA;
-    cudaError_t e = launch_split_kv_tc(p, s);
+    cudaError_t e = d == kDqk ? launch_split_kv_tc<576>(p, s) : launch_split_kv_tc<512>(p, s);
     if (e != cudaSuccess) return MLA_ERR_CUDA;
     if (ev_end && cudaEventRecord(ev_end, s) != cudaSuccess) return MLA_ERR_CUDA;
     e = launch_combine(p, s);

@@ -46,9 +46,12 @@ void carve_workspace(void *ws, int batch, int rows, int num_parts, float **o_acc
 
 cudaError_t launch_schedule(const int32_t *seqlens, int batch, int num_parts, int32_t *metadata,
                             int32_t *num_splits, unsigned int *status, cudaStream_t stream);
+// the tensor-core split-KV kernel for cached rows of width D (576 or 512)
+template <int D>
 cudaError_t launch_split_kv_tc(const DecodeParams &p, cudaStream_t stream);
 int split_kv_tc_tile_rows();
-// CTA pairs of the tensor-core split-KV kernel that fit on the current device at once
+// CTA pairs of the split-KV kernel for width D that fit on the current device at once
+template <int D>
 cudaError_t split_kv_tc_max_pairs(int *pairs);
 cudaError_t launch_combine(const DecodeParams &p, cudaStream_t stream);
 

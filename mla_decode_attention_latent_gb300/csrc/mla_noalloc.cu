@@ -62,7 +62,8 @@ extern "C" int mla_decode_kvcache_noalloc(const void *q, const void *kcache, int
     if (!q || !kcache || !block_table || !cache_seqlens || !tile_scheduler_metadata || !num_splits || !o || !lse)
         return MLA_ERR_INVALID_ARG;
     if (batch < 1 || s_q < 1 || h_q < 1 || h_kv < 1 || num_parts < 1 || d < 1 || dv < 1) return MLA_ERR_INVALID_ARG;
-    if (d != MLA_HEAD_DIM || dv != MLA_V_DIM || h_kv != 1 || (long long)s_q * h_q > 65536) return MLA_ERR_UNSUPPORTED;
+    if ((d != MLA_HEAD_DIM && d != MLA_V_DIM) || dv != MLA_V_DIM || h_kv != 1 || (long long)s_q * h_q > 65536)
+        return MLA_ERR_UNSUPPORTED;
     const size_t need = mla_workspace_bytes(batch, s_q, h_q, h_kv, dv, num_parts);
     if (need == 0) return MLA_ERR_INVALID_ARG;
     if (need > mla::kNoAllocScratchBytes) return MLA_ERR_WORKSPACE;  // beyond the fixed scratch

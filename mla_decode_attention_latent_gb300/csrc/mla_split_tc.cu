@@ -1,900 +1,7 @@
-// Split-KV MLA decode on sm_103a tensor cores: one CTA pair per (part, row tile).
-//
-// What is computed (per query row r = i * h_q + h of sequence b, over the keys
-// of the part's page range; see include/mla_decode.h):
-//   s_j = scale * <q_r, k_j>,  p_j = 2^(s_j log2 e - m),  O = sum_j p_j v_j / l
-// with an fp32 online softmax (running max m, running sum l), and at the end
-// of the range either the final O (bf16) and LSE, or an fp32 partial O and
-// partial LSE for the combine kernel when the sequence is split.  Sources:
-// "FlashMLA란 무엇인가?" (topnet.top article 5338), sections "FlashMLA의 주요
-// 특성" (bf16, paged cache, block 64) and "FlashMLA 설치 및 사용" step 3 (the
-// decode call returns o and lse); "Novita AI, H100 및 H200에서 FlashMLA 평가",
-// table "MHA vs MQA vs GQA vs MLA" (every head shares the latent KV row, so
-// QK^T and PV are dense contractions over all heads of a tile).
-//
-// Design (GB300-first; the pages' kernel is a Hopper design and only prior art):
-// a 128 x 512 fp32 output accumulator fills a whole SM's tensor memory, so the
-// work of one tile is split across the two CTAs of a cluster by role:
-//
-//   score CTA (rank 0)                       value CTA (rank 1)
-//   ------------------                       ------------------
-//   Q latent [128 x 512] bf16 in TMEM,       O tile [128 x 512] fp32 in TMEM
-//     Q RoPE [128 x 64] in smem              TMA: page dims 0..511 (8 chunks)
-//   TMA: 16 KB chunk slots, each holding       into a 2-stage ring
-//     one 64-dim chunk of two pages          tcgen05 O += P V  (N = 2 x 256)
-//   tcgen05 S = Q K^T over two pages at      4 warps: zero the tail rows of V,
-//     once (N = 128: full tensor rate)         lazy O rescale, epilogue staged
-//   4 warps: mask + online softmax; P and      through smem
-//     row factors -> local staging -> one
-//     bulk copy into the value CTA
-//
-// Loads: the score CTA's producer first streams whole pages (one contiguous
-// 72 KB each) from HBM into L2 with bulk prefetches, many pages ahead; the
-// chunk loads of both CTAs then hit L2, whose bandwidth is far above HBM's, so
-// the small shared-memory rings only have to cover L2 latency.  P and the row
-// factors (17 KB per page) go to the value CTA with one asynchronous bulk
-// copy that completes on the value CTA's barrier; the value CTA's MMA commit
-// hands the buffer back through a multicast commit.  The running max is
-// rescaled lazily: O is only corrected when a page's maximum exceeds the
-// current one by more than 2^8.
-//
-// Warp roles (256 threads): warp 0 issues TMA, warp 1 allocates TMEM and
-// issues MMAs (one elected lane), warps 2..5 are the row warps (thread t of
-// warp w owns TMEM lane / tile row 32 * (w % 4) + t); in the score CTA warp 6
-// is the second MMA issuer and warp 7 the second TMA producer.
-//
-// Every wait is bounded (mla_sm103.cuh); on a timeout the kernel raises
-// MLA_DEVERR_TIMEOUT, tells its peer CTA to stop, and unwinds.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-#include <cuda_runtime.h>
-#include <math_constants.h>
-
-#include <mutex>
-
-#include "mla_internal.h"
-#include "mla_sm103.cuh"
+// Split-KV kernel for the 576-wide latent cache (512 latent + 64 RoPE dims).
+#define MLA_SPLIT_D 576
+#include "mla_split_tc_impl.cuh"
 
 namespace mla {
-namespace {
-
-using namespace sm103;
-
-constexpr int kThreads = 256;                  // 8 warps: TMA, MMA, 4 row warps, second score MMA issuer and TMA producer
-constexpr int kTileRows = 128;                 // query rows per tile = TMEM lanes
-constexpr int kKSlots = 10;                    // score CTA: 16 KB chunk slots, two rings of 5
-constexpr int kScoreIssuers = 2;               // score-CTA MMA issuers (and TMA producers), alternating steps
-constexpr int kRingSlots = 10 / kScoreIssuers;  // slots per score-MMA issuer's ring
-constexpr int kVStages = 2;                    // value CTA ring: whole pages (dims 0..511)
-constexpr int kSBufs = 2;                      // S buffers in TMEM (score CTA), one per step of two pages
-constexpr int kPBufs = 2;                      // P buffers (staging in the score CTA, landing in the value CTA)
-constexpr int kKChunks = kDqk / 64;            // 9 chunks of 64 dims (128 B rows)
-constexpr int kVChunks = kDv / 64;             // 8
-constexpr int kLatChunks = kDv / 64;           // 8 latent chunks: the Q part kept in TMEM
-constexpr uint32_t kChunkBytes = kPage * 128;  // 64 tokens x 128 B = 8 KB
-constexpr uint32_t kSlotBytes = 2 * kChunkBytes;          // 16 KB: one chunk of two pages (128 token rows)
-constexpr uint32_t kVStageBytes = kVChunks * kChunkBytes;  // 64 KB
-constexpr uint32_t kPBytes = kTileRows * 128;             // 16 KB: 128 rows x 64 bf16, 128B-swizzled
-constexpr uint32_t kFacOff = kPBytes;                      // then fac[128] (fp32)
-constexpr uint32_t kInvLOff = kPBytes + kTileRows * 4;     // then inv_l[128] (fp32)
-constexpr uint32_t kPMsgBytes = kPBytes + 2 * kTileRows * 4;  // 17 KB, a multiple of 1 KB
-constexpr uint32_t kQCols = kDv / 2;                       // Q latent: 256 TMEM columns of bf16 pairs
-constexpr uint32_t kSCol0 = kQCols;                        // S buffers follow Q
-constexpr uint32_t kSCols = 2 * kPage;                     // an S buffer holds the scores of two pages
-constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleLog2 = 8.0f;                       // lazy rescale threshold (log2 units)
-constexpr uint32_t kEpiCols = 64;                          // epilogue chunk: 64 fp32 columns
-constexpr uint32_t kEpiStride = kEpiCols * 4 + 16;         // padded row stride (conflict-free v4 stores)
-
-// shared-memory layout (offsets from the 1024-byte aligned base)
-// score CTA: [K rings 2 x 5 x 16 KB][Q RoPE tile 16 KB][P staging 2 x 17 KB]
-constexpr uint32_t kKRingOff = 0;
-constexpr uint32_t kQRopeOff = kKRingOff + kKSlots * kSlotBytes;
-constexpr uint32_t kStageOff = kQRopeOff + kTileRows * 128;
-constexpr uint32_t kScoreEnd = kStageOff + kPBufs * kPMsgBytes;
-// value CTA: [V ring 2 x 64 KB][P landing 2 x 17 KB][epilogue staging 34 KB]
-constexpr uint32_t kVRingOff = 0;
-constexpr uint32_t kPBufOff = kVRingOff + kVStages * kVStageBytes;
-constexpr uint32_t kEpiOff = kPBufOff + kPBufs * kPMsgBytes;
-constexpr uint32_t kValueEnd = kEpiOff + kTileRows * kEpiStride;
-// barriers at the same offset in both CTAs (the peer arrives on some of them)
-constexpr uint32_t kBarOff = ((kScoreEnd > kValueEnd ? kScoreEnd : kValueEnd) + 1023u) & ~1023u;
-static_assert(kQRopeOff % 1024 == 0 && kStageOff % 1024 == 0 && kPBufOff % 1024 == 0 && kPMsgBytes % 1024 == 0,
-              "swizzled tiles need 1 KB alignment");
-
-enum Bar {
-    // score CTA
-    B_KFULL = 0, B_KEMPTY = B_KFULL + kKSlots, B_SFULL = B_KEMPTY + kKSlots, B_SEMPTY = B_SFULL + kSBufs,
-    B_QFULL = B_SEMPTY + kSBufs, B_QACK = B_QFULL + 1, B_PFREE = B_QACK + 1,
-    // value CTA
-    B_VFULL = B_PFREE + kPBufs, B_VEMPTY = B_VFULL + kVStages, B_PFULL = B_VEMPTY + kVStages,
-    B_PREADY = B_PFULL + kPBufs, B_PVDONE = B_PREADY + kPBufs, B_ODONE = B_PVDONE + 1, B_OEMPTY = B_ODONE + 1,
-    // both
-    B_FINAL = B_OEMPTY + 1, B_COUNT = B_FINAL + 1
-};
-constexpr uint32_t kTmemSlotOff = kBarOff + B_COUNT * 8;
-constexpr uint32_t kAbortOff = kTmemSlotOff + 4;
-constexpr uint32_t kSmemUsed = kAbortOff + 4;
-constexpr size_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack of the dynamic base
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-static_assert(kRingSlots * kScoreIssuers == kKSlots && kSBufs % kScoreIssuers == 0, "one K ring per score-MMA issuer");
-
-// -------------------------------------------------------------- work walk
-struct Segment {
-    int b, T, n_pages, p0, p1, split, n_split;
-};
-
-struct PartWalk {
-    int bb, bp, eb, ep, bs, b;
-    __device__ void init(const DecodeParams &p, int part) {
-        const int32_t *md = p.metadata + (size_t)part * kMdInts;
-        bb = md[0];
-        bp = md[1];
-        eb = md[2];
-        ep = md[3];
-        bs = md[4];
-        b = (bb == eb && bp == ep) ? p.batch : bb;  // an empty part walks nothing
-        if (b < 0) b = p.batch;
-    }
-    __device__ bool next(const DecodeParams &p, Segment &s) {
-        if (b >= p.batch || b > eb || (b == eb && ep == 0)) return false;
-        int T = p.seqlens[b];
-        if (T < 0) T = 0;
-        if (T > p.max_blocks * kPage) T = p.max_blocks * kPage;
-        s.b = b;
-        s.T = T;
-        s.n_pages = (T + kPage - 1) / kPage;
-        s.p1 = (b == eb) ? min(ep, s.n_pages) : s.n_pages;
-        s.p0 = (b == bb) ? min(bp, s.p1) : 0;
-        s.split = (b == bb) ? bs : 0;
-        s.n_split = p.num_splits[b + 1] - p.num_splits[b];
-        ++b;
-        return true;
-    }
-};
-
-struct Ctx {
-    uint8_t *base;
-    uint64_t *bars;
-    volatile int *abort_flag;
-    unsigned int *status;
-    uint32_t peer;  // the other CTA's rank
-    __device__ uint64_t *bar(int i) const { return bars + i; }
-};
-
-// bounded wait that also gives up when this CTA was told to abort
-template <bool kCluster = false>
-__device__ __forceinline__ bool wait(const Ctx &c, int bar_idx, uint32_t parity) {
-    const uint32_t a = smem_u32(c.bar(bar_idx));
-    if (kCluster ? mbar_test_cluster(a, parity) : mbar_test(a, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
-        for (int i = 0; i < 32; ++i)
-            if (kCluster ? mbar_test_cluster(a, parity) : mbar_test(a, parity)) return true;
-        if (*c.abort_flag) return false;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
-            atomicOr(c.status, MLA_DEVERR_TIMEOUT);
-            *c.abort_flag = 1;
-            // tell the peer CTA to stop waiting on us
-            asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(mapa(smem_u32((const void *)c.abort_flag), c.peer)),
-                         "r"(1)
-                         : "memory");
-            return false;
-        }
-    }
-}
-
-// the same wait taken by every lane of a warp, with one outcome for all of
-// them (the row warps run warp-collective tcgen05.ld/st after their waits)
-template <bool kCluster = false>
-__device__ __forceinline__ bool warp_wait(const Ctx &c, int bar_idx, uint32_t parity) {
-    return __all_sync(0xffffffffu, wait<kCluster>(c, bar_idx, parity));
-}
-
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-__device__ __forceinline__ int safe_block(const DecodeParams &p, int b, int page) {
-    const int blk = p.block_table[(size_t)b * p.max_blocks + page];
-    if (blk < 0 || (int64_t)blk >= p.num_blocks) {
-        atomicOr(p.status, MLA_DEVERR_BLOCK_ID);
-        return 0;
-    }
-    return blk;
-}
-
-// -------------------------------------------------------------- roles
-// Score-CTA TMA producers (one lane each, one per MMA issuer's ring `r`,
-// taking the steps of parity r).  A step is up to two consecutive pages
-// of a segment; each of a step's 9 64-dim chunks is one 16 KB ring slot
-// holding 128 token rows (first page rows 0-63, second page rows 64-127), so
-// that one tcgen05 MMA with N = 128 covers both pages.  Producer 0 first asks
-// L2 for the Q rows of every segment.  (Streaming whole pages into L2 ahead
-// of the chunk loads, from either CTA and at any distance tried, measured
-// slower on GB300 than letting the chunk loads fetch them.)
-__device__ void score_producer(const DecodeParams &p, const Ctx &c, const CUtensorMap *map, int part, int tile,
-                               int r) {
-    PartWalk walk;
-    Segment s;
-    {
-        // the block-table line of the part's first page travels while the
-        // walk reads the sequence lengths (one dependent round trip fewer
-        // before the first chunk load)
-        const int32_t *md = p.metadata + (size_t)part * kMdInts;
-        const int bb = md[0], bp = md[1];
-        if (bb >= 0 && bb < p.batch && bp >= 0 && bp < p.max_blocks)
-            prefetch_line_l1(p.block_table + (size_t)bb * p.max_blocks + bp);
-    }
-    if (r == 0) {
-        const int rows = min(kTileRows, p.rows - tile * kTileRows);
-        walk.init(p, part);
-        while (walk.next(p, s))
-            if (s.p1 > s.p0 && rows > 0)
-                prefetch_l2(p.q + ((size_t)s.b * p.rows + (size_t)tile * kTileRows) * kDqk, (uint32_t)rows * kDqk * 2);
-    }
-    walk.init(p, part);
-    uint32_t ring_it = 0;  // chunks issued into this producer's ring
-    uint32_t step = 0;
-    bool ok = true;
-    while (ok && walk.next(p, s)) {
-        for (int pg = s.p0; ok && pg < s.p1; pg += 2, ++step) {
-            const int npg = min(2, s.p1 - pg);
-            if ((int)(step % kScoreIssuers) != r) continue;  // the other ring's step
-            const int blk0 = safe_block(p, s.b, pg);
-            const int blk1 = npg > 1 ? safe_block(p, s.b, pg + 1) : 0;
-            for (int ch = 0; ch < kKChunks; ++ch) {
-                const uint32_t k = ring_it++;
-                const int sl = r * kRingSlots + (int)(k % kRingSlots);
-                if (!wait(c, B_KEMPTY + sl, ((k / kRingSlots) & 1) ^ 1)) {
-                    ok = false;
-                    break;
-                }
-                uint8_t *dst = c.base + kKRingOff + sl * kSlotBytes;
-                mbar_arrive_expect_tx(c.bar(B_KFULL + sl), npg * kChunkBytes);
-                tma_load_3d(dst, map, c.bar(B_KFULL + sl), 64 * ch, 0, blk0);
-                if (npg > 1) tma_load_3d(dst + kChunkBytes, map, c.bar(B_KFULL + sl), 64 * ch, 0, blk1);
-            }
-        }
-    }
-    // the last loads must have landed before this CTA may exit (already true
-    // on the normal path, where the MMAs consumed them)
-    for (uint32_t k = ring_it > (uint32_t)kRingSlots ? ring_it - kRingSlots : 0; k < ring_it; ++k)
-        mbar_wait(c.bar(B_KFULL + r * kRingSlots + (int)(k % kRingSlots)), (k / kRingSlots) & 1, c.status);
-}
-
-// Value-CTA TMA producer (one lane): whole pages (dims 0..511) through the V ring.
-__device__ void value_producer(const DecodeParams &p, const Ctx &c, const CUtensorMap *map, int part) {
-    PartWalk walk;
-    Segment s;
-    walk.init(p, part);
-    uint32_t it = 0;
-    bool ok = true;
-    while (ok && walk.next(p, s)) {
-        for (int pg = s.p0; pg < s.p1; ++pg, ++it) {
-            const int st = it % kVStages;
-            if (!wait(c, B_VEMPTY + st, ((it / kVStages) & 1) ^ 1)) {
-                ok = false;
-                break;
-            }
-            const int blk = safe_block(p, s.b, pg);
-            mbar_arrive_expect_tx(c.bar(B_VFULL + st), kVStageBytes);
-            uint8_t *dst = c.base + kVRingOff + st * kVStageBytes;
-            for (int ch = 0; ch < kVChunks; ++ch)
-                tma_load_3d(dst + ch * kChunkBytes, map, c.bar(B_VFULL + st), 64 * ch, 0, blk);
-        }
-    }
-    for (uint32_t k = it > (uint32_t)kVStages ? it - kVStages : 0; k < it; ++k)
-        mbar_wait(c.bar(B_VFULL + (int)(k % kVStages)), (k / kVStages) & 1, c.status);
-}
-
-// Score-CTA MMA issuers: S[buf] = Q K^T for every step of (up to) two pages:
-// the 512 latent dims with A = Q from TMEM, the 64 RoPE dims with A = the
-// Q RoPE tile in shared memory; B = the 128 (or 64) token rows of each slot.
-// A tcgen05.mma holds its issuing thread for about its own execution time, so
-// whatever that thread does between MMAs (barrier waits, commits, loop
-// bookkeeping) leaves the tensor pipe idle.  Two issuers therefore alternate
-// steps by global step index (`lane` 0: even steps into S buffer 0, 1: odd
-// steps into buffer 1): one's bookkeeping overlaps the other's MMAs.  Each
-// issuer has its own ring of chunk slots, filled in step order by the
-// producer and consumed in order by its only consumer: with a shared ring, an
-// issuer could test a slot's barrier for a later phase while the other
-// issuer's earlier chunk in that slot had not landed, which parity waits
-// cannot tell apart.  Both issuers also wait for every segment's Q, so that
-// their view of the Q barrier's phases stays exact.
-__device__ void score_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, int part, int lane) {
-    PartWalk walk;
-    walk.init(p, part);
-    Segment s;
-    uint32_t step = 0, seg = 0, ring_it = 0;  // ring_it: chunks consumed from this issuer's own ring
-    const uint32_t ring = smem_u32(c.base + kKRingOff);
-    const uint64_t rope_desc = desc_sw128(smem_u32(c.base + kQRopeOff), 16, 1024);
-    while (walk.next(p, s)) {
-        const int nsteps = (s.p1 - s.p0 + 1) / 2;
-        if (!wait(c, B_QFULL, seg & 1)) return;  // Q of this segment is in TMEM and smem
-        tc_fence_after();
-        mbar_arrive(c.bar(B_QACK));              // the row warps may load the next Q only after both issuers saw this one
-        ++seg;
-        for (int j = 0; j < nsteps; ++j) {
-            const uint32_t st = step + j;       // global step index
-            if ((int)(st % kScoreIssuers) != lane) continue;
-            const int sb = (int)(st % kSBufs);
-            const uint32_t d = tmem + kSCol0 + sb * kSCols;
-            const int npg = min(2, s.p1 - (s.p0 + 2 * j));
-            const uint32_t idesc = npg == 2 ? idesc_bf16(kTileRows, 2 * kPage, false, false)
-                                            : idesc_bf16(kTileRows, kPage, false, false);
-            if (!wait(c, B_SEMPTY + sb, ((st / kSBufs) & 1) ^ 1)) return;
-            tc_fence_after();  // the row warps' reads of this S buffer come first
-            for (int ch = 0; ch < kKChunks; ++ch, ++ring_it) {
-                const uint32_t sl = lane * kRingSlots + ring_it % kRingSlots;
-                // TMA data: the barrier's completion already orders it before
-                // the MMA's reads (no tcgen05 fence here: it would drain the pipe)
-                if (!wait(c, B_KFULL + sl, (ring_it / kRingSlots) & 1)) return;
-                const uint64_t bd = desc_sw128(ring + sl * kSlotBytes, 16, 1024);
-                if (ch < kLatChunks) {
-                    const uint32_t a = tmem + ch * 32;
-                    mma_ts(d, a, bd, idesc, ch != 0);
-                    mma_ts(d, a + 8, bd + 2, idesc, 1u);   // +32 B along K: descriptor address field +2
-                    mma_ts(d, a + 16, bd + 4, idesc, 1u);
-                    mma_ts(d, a + 24, bd + 6, idesc, 1u);
-                } else {
-                    mma_ss(d, rope_desc, bd, idesc, 1u);
-                    mma_ss(d, rope_desc + 2, bd + 2, idesc, 1u);
-                    mma_ss(d, rope_desc + 4, bd + 4, idesc, 1u);
-                    mma_ss(d, rope_desc + 6, bd + 6, idesc, 1u);
-                }
-                mma_commit(c.bar(B_KEMPTY + sl));
-            }
-            mma_commit(c.bar(B_SFULL + sb));
-        }
-        step += nsteps;
-    }
-}
-
-// Value-CTA MMA issuer: O (+)= P V for every page.  Only segments with pages
-// touch O, so only they count on the O barriers: the epilogue of a segment
-// without pages never waits on this thread, and counting it would let the row
-// warps complete two phases of the O-free barrier between two of its waits.
-__device__ void value_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, int part) {
-    constexpr uint32_t idesc = idesc_bf16(kTileRows, 256, false, true);
-    PartWalk walk;
-    walk.init(p, part);
-    Segment s;
-    uint32_t it = 0, oseg = 0;  // oseg: segments with pages so far
-    while (walk.next(p, s)) {
-        if (s.p1 <= s.p0) continue;
-        if (!wait(c, B_OEMPTY, (oseg & 1) ^ 1)) return;  // previous segment's epilogue has read O
-        ++oseg;
-        for (int pg = s.p0; pg < s.p1; ++pg, ++it) {
-            const int st = it % kVStages, pb = it % kPBufs;
-            if (!wait(c, B_VFULL + st, (it / kVStages) & 1)) return;
-            if (!wait(c, B_PREADY + pb, (it / kPBufs) & 1)) return;
-            tc_fence_after();
-            const uint32_t vtile = smem_u32(c.base + kVRingOff + st * kVStageBytes);
-            const uint32_t ptile = smem_u32(c.base + kPBufOff + pb * kPMsgBytes);
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int k = 0; k < kPage / 16; ++k) {
-                    const uint64_t ad = desc_sw128(ptile + k * 32, 16, 1024);
-                    const uint64_t bd = desc_sw128(vtile + h * 4 * kChunkBytes + k * 2048, kChunkBytes, 1024);
-                    mma_ss(tmem + h * 256, ad, bd, idesc, (pg > s.p0 || k > 0) ? 1u : 0u);
-                }
-            mma_commit(c.bar(B_VEMPTY + st));
-            mma_commit(c.bar(B_PVDONE));
-            if (pg == s.p1 - 1) mma_commit(c.bar(B_ODONE));  // O of the segment is complete
-            mma_commit_multicast(c.bar(B_PFREE + pb), (uint16_t)(1u << c.peer));
-        }
-    }
-}
-
-// Score-CTA row warps: Q -> TMEM and smem, masked online softmax, P and row
-// factors -> staging -> bulk copies into the value CTA, each warp sending its
-// own 32 rows as soon as they are staged.
-__device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, int part, int tile) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = 32 * (warp & 3) + lane;                // tile row = TMEM lane
-    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    const int gr = tile * kTileRows + r;                 // row within the sequence's rows
-    const bool row_ok = gr < p.rows;
-    const int qi = row_ok ? gr / p.h_q : 0;              // query token index
-    const uint32_t peer_buf = mapa(smem_u32(c.base + kPBufOff), c.peer);
-    const uint32_t peer_pfull = mapa(smem_u32(c.bar(B_PFULL)), c.peer);
-    PartWalk walk;
-    walk.init(p, part);
-    Segment s;
-    uint32_t it = 0, step = 0, seg = 0;
-    while (walk.next(p, s)) {
-        const int T_row = p.causal ? s.T - p.s_q + qi + 1 : s.T;
-        // both MMA issuers have seen the previous segment's Q (and, having
-        // consumed all its S buffers, the MMAs reading it are done)
-        if (seg > 0 && !warp_wait(c, B_QACK, (seg - 1) & 1)) return;
-        ++seg;
-        if (s.p1 > s.p0) {
-            // Q row r: latent dims 0..511 into TMEM lane r (columns 0..255,
-            // bf16 pairs), RoPE dims 512..575 into row r of the swizzled smem
-            // tile; four 64-dim chunks (32 loads) in flight at a time
-            const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q + ((size_t)s.b * p.rows + (row_ok ? gr : 0)) * kDqk);
-#pragma unroll 1
-            for (int ch0 = 0; ch0 < kLatChunks; ch0 += 4) {
-                uint4 x[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) x[j] = row_ok ? __ldg(qrow + ch0 * 8 + j) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    uint32_t v[32];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        v[4 * j] = x[8 * k + j].x;
-                        v[4 * j + 1] = x[8 * k + j].y;
-                        v[4 * j + 2] = x[8 * k + j].z;
-                        v[4 * j + 3] = x[8 * k + j].w;
-                    }
-                    tmem_st32(tmem + lane_base + (ch0 + k) * 32, v);
-                }
-            }
-            uint4 *rope = reinterpret_cast<uint4 *>(c.base + kQRopeOff + r * 128);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) rope[j ^ (r & 7)] = row_ok ? __ldg(qrow + kLatChunks * 8 + j) : make_uint4(0, 0, 0, 0);
-            fence_proxy_async_smem();
-            tmem_wait_st();
-        }
-        tc_fence_before();
-        mbar_arrive(c.bar(B_QFULL));
-
-        float m = -CUDART_INF_F, l = 0.f;
-        for (int pg = s.p0; pg < s.p1; ++pg, ++it) {
-            const int pb = it % kPBufs;
-            const int q2 = (pg - s.p0) & 1;          // position of this page in its step
-            const int sb = step % kSBufs;
-            if (q2 == 0 && !warp_wait(c, B_SFULL + sb, (step / kSBufs) & 1)) return;
-            tc_fence_after();
-            uint32_t sr[64];
-            {
-                uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[0]);
-                uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sr[32]);
-                tmem_ld32(tmem + lane_base + kSCol0 + sb * kSCols + q2 * kPage, lo);
-                tmem_ld32(tmem + lane_base + kSCol0 + sb * kSCols + q2 * kPage + 32, hi);
-            }
-            tmem_wait_ld();
-            if (q2 == 1 || pg == s.p1 - 1) {         // last page of the step: release its S buffer
-                tc_fence_before();
-                mbar_arrive(c.bar(B_SEMPTY + sb));
-                ++step;
-            }
-
-            // keys of this page visible to this row
-            int nvalid = row_ok ? T_row - pg * kPage : 0;
-            nvalid = nvalid < 0 ? 0 : (nvalid > kPage ? kPage : nvalid);
-            const float sc = p.scale_log2;
-            // page maximum of scale * log2(e) * s over the visible keys, four
-            // independent chains to keep the dependency depth short.  A full
-            // page with a positive scale takes the maximum of the raw scores
-            // (scaling is monotone there) and folds the scale into one FMA per
-            // exponent below; otherwise the scaled, masked scores (-inf past
-            // the visible keys) replace the raw ones and the FMA scale is 1.
-            const bool raw = nvalid == kPage && sc > 0.f;
-            const float fsc = raw ? sc : 1.f;
-            float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
-            if (!raw) {
-#pragma unroll
-                for (int j = 0; j < 64; ++j)
-                    sr[j] = __float_as_uint((j < nvalid) ? __uint_as_float(sr[j]) * sc : -CUDART_INF_F);
-            }
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                mx4[j & 3] = max3f(mx4[j & 3], __uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1]));
-            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * fsc;
-            float fac = 1.f;
-            if (mx > m + kRescaleLog2 || (m == -CUDART_INF_F && mx > -CUDART_INF_F)) {
-                fac = ex2(m - mx);  // 0 when m was -inf
-                m = mx;
-            }
-            // exponent inputs and the row sum two lanes per instruction
-            uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
-            uint32_t pk[32];
-            if (m == -CUDART_INF_F) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) pk[j] = 0u;
-            } else {
-                const uint64_t sc2 = f2_pack(fsc, fsc), nm2 = f2_pack(-m, -m);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    float xa, xb;
-                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1])), sc2, nm2), xa, xb);
-                    const float a = ex2(xa), b = ex2(xb);
-                    sum2[j & 3] = f2_add(sum2[j & 3], f2_pack(a, b));
-                    pk[j] = pack_bf16(a, b);
-                }
-            }
-            float sum_lo, sum_hi;
-            f2_unpack(f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3])), sum_lo, sum_hi);
-            const float sum = sum_lo + sum_hi;
-            l = l * fac + sum;
-
-            // staging pb is free once the value CTA's MMA of page it - 2 is
-            // done: that MMA consumed the bulk copy made from it
-            if (!warp_wait<true>(c, B_PFREE + pb, ((it / kPBufs) & 1) ^ 1)) return;
-            uint8_t *stage = c.base + kStageOff + pb * kPMsgBytes;
-            const uint32_t stage_s = smem_u32(stage);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                sts128(stage_s + r * 128 + 16 * (j ^ (r & 7)), pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-            sts32(stage_s + kFacOff + 4 * r, __float_as_uint(fac));
-            if (pg == s.p1 - 1) sts32(stage_s + kInvLOff + 4 * r, __float_as_uint(l > 0.f ? 1.f / l : 0.f));
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                // this warp's 32 rows of P and of the row factors; the bulk
-                // copies' completion on the same barrier makes them visible
-                const bool last = pg == s.p1 - 1;
-                const uint32_t bar = peer_pfull + pb * 8;
-                const uint32_t rows_off = (uint32_t)(32 * (warp & 3)) * 128, fac_off = (uint32_t)(32 * (warp & 3)) * 4;
-                const uint32_t dst = peer_buf + pb * kPMsgBytes;
-                mbar_arrive_expect_tx_remote_relaxed(bar, 32 * 128 + (last ? 2 : 1) * 32 * 4);
-                bulk_copy_to_peer(dst + rows_off, stage + rows_off, 32 * 128, bar);
-                bulk_copy_to_peer(dst + kFacOff + fac_off, stage + kFacOff + fac_off, 32 * 4, bar);
-                if (last) bulk_copy_to_peer(dst + kInvLOff + fac_off, stage + kInvLOff + fac_off, 32 * 4, bar);
-            }
-        }
-        // LSE of this row over the segment (natural log)
-        if (row_ok) {
-            const float lse_row = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
-            if (s.n_split <= 1) {
-                p.lse[(size_t)s.b * p.rows + gr] = lse_row;
-            } else {
-                const int slot = p.num_splits[s.b] + s.split;
-                if (slot >= 0 && slot < p.max_splits) p.lse_accum[(size_t)slot * p.rows + gr] = lse_row;
-                else atomicOr(p.status, MLA_DEVERR_SEQLEN);
-            }
-        }
-    }
-    // the peer's last commits arrive on our P-free barriers: let them land
-    // before this CTA can leave (this also covers the last bulk copies)
-    for (uint32_t k = it > (uint32_t)kPBufs ? it - kPBufs : 0; k < it; ++k)
-        if (!warp_wait<true>(c, B_PFREE + (int)(k % kPBufs), (k / kPBufs) & 1)) return;
-}
-
-// Value-CTA row warps: V tail zeroing, lazy O rescale, epilogue.
-__device__ void value_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, int part, int tile) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = 32 * (warp & 3) + lane;
-    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-    const int tid = threadIdx.x - 64;  // 0..127 among the row warps
-    const uint32_t epi_s = smem_u32(c.base + kEpiOff);
-    PartWalk walk;
-    walk.init(p, part);
-    Segment s;
-    uint32_t it = 0, oseg = 0;  // oseg: segments with pages so far
-    while (walk.next(p, s)) {
-        float inv_l = 0.f;
-        for (int pg = s.p0; pg < s.p1; ++pg, ++it) {
-            const int pb = it % kPBufs, st = it % kVStages;
-            if (!warp_wait<true>(c, B_PFULL + pb, (it / kPBufs) & 1)) return;
-            const uint32_t buf_s = smem_u32(c.base + kPBufOff + pb * kPMsgBytes);
-            const float fac = __uint_as_float(lds32(buf_s + kFacOff + 4 * r));
-            if (pg == s.p1 - 1) inv_l = __uint_as_float(lds32(buf_s + kInvLOff + 4 * r));
-            // rows past the sequence's end in its last page: zero them in V so
-            // that garbage (even NaN) times a zero weight stays zero
-            const int tail = s.T - pg * kPage;
-            if (tail < kPage) {
-                if (!warp_wait(c, B_VFULL + st, (it / kVStages) & 1)) return;
-                uint8_t *vt = c.base + kVRingOff + st * kVStageBytes;
-                const int rows_bad = kPage - tail;
-                for (int idx = tid; idx < kVChunks * rows_bad * 8; idx += 128) {
-                    const int ch = idx / (rows_bad * 8);
-                    const int rr = tail + (idx / 8) % rows_bad;
-                    const int piece = idx % 8;
-                    *reinterpret_cast<uint4 *>(vt + ch * kChunkBytes + rr * 128 + piece * 16) = make_uint4(0, 0, 0, 0);
-                }
-                fence_proxy_async_smem();
-            }
-            // lazy rescale of this row of O before the next accumulation
-            const bool need = (pg > s.p0) && (fac != 1.f);
-            if (__any_sync(0xffffffffu, need)) {
-                if (!warp_wait(c, B_PVDONE, (it - 1) & 1)) return;  // every earlier P V has landed
-                tc_fence_after();
-#pragma unroll 1
-                for (int ch = 0; ch < 16; ++ch) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + lane_base + ch * 32, v);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * fac);
-                    tmem_st32(tmem + lane_base + ch * 32, v);
-                }
-                tmem_wait_st();
-            }
-            tc_fence_before();
-            mbar_arrive(c.bar(B_PREADY + pb));
-        }
-        // epilogue: O / l -> bf16 output, or fp32 partial for the combine.
-        // Each 64-column chunk goes TMEM -> registers -> smem (row per
-        // thread), then the warp writes its 32 whole rows with coalesced stores.
-        const bool has_pages = s.p1 > s.p0;
-        if (has_pages) {
-            // every P V of the segment has landed.  (The per-page barrier
-            // cannot serve here: the row warps only know that the MMA of page
-            // it - 3 is done, and a parity wait cannot tell phase it - 1 from
-            // phase it - 3.)
-            if (!warp_wait(c, B_ODONE, oseg & 1)) return;
-            ++oseg;
-            tc_fence_after();
-        }
-        const bool split = s.n_split > 1;
-        int slot = 0;
-        if (split) {
-            slot = p.num_splits[s.b] + s.split;
-            if (slot < 0 || slot >= p.max_splits) {
-                if (tid == 0) atomicOr(p.status, MLA_DEVERR_SEQLEN);
-                slot = -1;
-            }
-        }
-        // each warp stores the 32 rows of its own TMEM lane quarter, through
-        // its own slice of the staging tile: no cross-warp barrier is needed
-        const int wrow0 = 32 * (warp & 3);
-#pragma unroll 1
-        for (int ch = 0; ch < kDv / (int)kEpiCols; ++ch) {
-            uint32_t v[64];
-            if (has_pages) {
-                uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
-                uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
-                tmem_ld32(tmem + lane_base + ch * kEpiCols, lo);
-                tmem_ld32(tmem + lane_base + ch * kEpiCols + 32, hi);
-                tmem_wait_ld();
-                if (ch == kDv / (int)kEpiCols - 1) {  // the last TMEM read: O may be overwritten now
-                    tc_fence_before();
-                    mbar_arrive(c.bar(B_OEMPTY));
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 64; ++j) v[j] = 0u;
-            }
-            const uint32_t srow = epi_s + r * kEpiStride;
-            if (split) {  // fp32 partial: 256 B of the row
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    sts128(srow + 16 * j, __float_as_uint(__uint_as_float(v[4 * j]) * inv_l),
-                           __float_as_uint(__uint_as_float(v[4 * j + 1]) * inv_l),
-                           __float_as_uint(__uint_as_float(v[4 * j + 2]) * inv_l),
-                           __float_as_uint(__uint_as_float(v[4 * j + 3]) * inv_l));
-            } else {  // bf16 output: 128 B of the row
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    sts128(srow + 16 * j,
-                           pack_bf16(__uint_as_float(v[8 * j]) * inv_l, __uint_as_float(v[8 * j + 1]) * inv_l),
-                           pack_bf16(__uint_as_float(v[8 * j + 2]) * inv_l, __uint_as_float(v[8 * j + 3]) * inv_l),
-                           pack_bf16(__uint_as_float(v[8 * j + 4]) * inv_l, __uint_as_float(v[8 * j + 5]) * inv_l),
-                           pack_bf16(__uint_as_float(v[8 * j + 6]) * inv_l, __uint_as_float(v[8 * j + 7]) * inv_l));
-            }
-            __syncwarp();
-            if (slot >= 0) {
-                // all of the warp's shared loads first, then its global stores
-                uint4 x[16];
-                if (split) {
-                    // fp32: 256 B per row chunk, two rows per warp store
-#pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        x[k] = lds128(epi_s + (wrow0 + 2 * k + (lane >> 4)) * kEpiStride + 16 * (lane & 15));
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        const int g = tile * kTileRows + wrow0 + 2 * k + (lane >> 4);
-                        if (g < p.rows)
-                            reinterpret_cast<uint4 *>(p.o_accum + ((size_t)slot * p.rows + g) * kDv + ch * kEpiCols)[lane & 15] = x[k];
-                    }
-                } else {
-                    // bf16: 128 B per row chunk, four rows per warp store
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        x[k] = lds128(epi_s + (wrow0 + 4 * k + (lane >> 3)) * kEpiStride + 16 * (lane & 7));
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int g = tile * kTileRows + wrow0 + 4 * k + (lane >> 3);
-                        if (g < p.rows)
-                            reinterpret_cast<uint4 *>(p.o + ((size_t)s.b * p.rows + g) * kDv + ch * kEpiCols)[lane & 7] = x[k];
-                    }
-                }
-            }
-            __syncwarp();  // the slice is rewritten by the next chunk
-        }
-    }
-}
-
-
-
-
-// -------------------------------------------------------------- kernel
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t rank = cluster_ctarank();
-    const bool is_score = rank == 0;
-    const int part = blockIdx.x >> 1;
-    const int tile = blockIdx.y;
-    const int warp = threadIdx.x >> 5;
-
-    Ctx c;
-    c.base = base;
-    c.bars = reinterpret_cast<uint64_t *>(base + kBarOff);
-    c.abort_flag = reinterpret_cast<volatile int *>(base + kAbortOff);
-    c.status = p.status;
-    c.peer = rank ^ 1u;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + kTmemSlotOff);
-
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kKSlots; ++i) {
-            mbar_init(c.bar(B_KFULL + i), 1);
-            mbar_init(c.bar(B_KEMPTY + i), 1);
-        }
-        for (int i = 0; i < kVStages; ++i) {
-            mbar_init(c.bar(B_VFULL + i), 1);
-            mbar_init(c.bar(B_VEMPTY + i), 1);
-        }
-        for (int i = 0; i < kSBufs; ++i) {
-            mbar_init(c.bar(B_SFULL + i), 1);
-            mbar_init(c.bar(B_SEMPTY + i), 128);
-        }
-        mbar_init(c.bar(B_QFULL), 128);
-        mbar_init(c.bar(B_QACK), kScoreIssuers);  // every score-MMA issuer has seen a segment's Q
-        for (int i = 0; i < kPBufs; ++i) {
-            mbar_init(c.bar(B_PFREE + i), 1);
-            mbar_init(c.bar(B_PFULL + i), 4);  // one arrival per row warp of the score CTA
-            mbar_init(c.bar(B_PREADY + i), 128);
-        }
-        mbar_init(c.bar(B_PVDONE), 1);
-        mbar_init(c.bar(B_ODONE), 1);
-        mbar_init(c.bar(B_OEMPTY), 128);
-        mbar_init(c.bar(B_FINAL), is_score ? kScoreIssuers : 1);  // one commit per MMA issuer
-        *c.abort_flag = 0;
-        fence_mbar_init();
-        tma_prefetch_desc(&kv_map);
-    }
-    if (warp == 1) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    cluster_arrive();
-    cluster_wait();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    // Everything above touches only this CTA's shared memory, TMEM and the
-    // kernel parameters, so it overlaps the previous kernel's tail when the
-    // launch is programmatic; no global memory is read or written before this.
-    // (This kernel never triggers its own dependents early: doing so, at the
-    // start or after the last page, measured 1-4 % slower on GB300; the
-    // combine launch then follows this grid's completion.)
-    griddep_wait();
-
-    if (warp == 0 || warp == 7) {
-        if (elect_one_lane() && (warp == 0 || (is_score && kScoreIssuers > 1))) {
-            if (is_score) score_producer(p, c, &kv_map, part, tile, warp == 0 ? 0 : 1);
-            else value_producer(p, c, &kv_map, part);
-        }
-    } else if (warp == 1 || warp == 6) {
-        if (elect_one_lane() && (warp == 1 || (is_score && kScoreIssuers > 1))) {
-            if (is_score) score_mma(p, c, tmem, part, warp == 1 ? 0 : 1);
-            else value_mma(p, c, tmem, part);
-            // all MMAs this thread issued must finish before TMEM is released
-            mma_commit(c.bar(B_FINAL));
-            mbar_wait(c.bar(B_FINAL), 0, c.status);
-        }
-        __syncwarp();
-    } else {
-        if (is_score) score_rows(p, c, tmem, part, tile);
-        else value_rows(p, c, tmem, part, tile);
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    // neither CTA may leave while its peer can still touch its shared memory
-    cluster_arrive();
-    cluster_wait();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
-    }
-}
-
-// -------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    });
-    return fn;
-}
-
-// kcache [num_blocks][64][576] bf16 viewed as a 3-D tensor {576, 64, num_blocks};
-// one box is a 64-dim x 64-token chunk, stored with the 128-byte swizzle that
-// the tcgen05 K-major (K) and MN-major (V) operand descriptors expect.
-bool make_kv_map(CUtensorMap *m, const void *kcache, int64_t num_blocks) {
-    auto enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)kDqk, (cuuint64_t)kPage, (cuuint64_t)num_blocks};
-    cuuint64_t strides[2] = {(cuuint64_t)kDqk * 2, (cuuint64_t)kPage * kDqk * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)kPage, 1};
-    cuuint32_t es[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(kcache), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-constexpr int kMaxDevices = 64;
-bool g_attr_set[kMaxDevices] = {};
-std::mutex g_attr_mutex;
-
-cudaError_t prepare(int dev) {
-    std::lock_guard<std::mutex> lock(g_attr_mutex);
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if (g_attr_set[dev]) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(split_kv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    if (e == cudaSuccess) g_attr_set[dev] = true;
-    return e;
-}
-
-}  // namespace
-
-int split_kv_tc_tile_rows() { return kTileRows; }
-
-cudaError_t split_kv_tc_max_pairs(int *pairs) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if ((e = prepare(dev)) != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = 2;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    cfg.numAttrs = 0;  // the cluster shape is fixed by the kernel's attribute
-    e = cudaOccupancyMaxActiveClusters(&n, split_kv_tc_kernel, &cfg);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        cfg.numAttrs = 1;
-        e = cudaOccupancyMaxActiveClusters(&n, split_kv_tc_kernel, &cfg);
-    }
-    if (e != cudaSuccess) return e;
-    *pairs = n;
-    return cudaSuccess;
-}
-
-cudaError_t launch_split_kv_tc(const DecodeParams &p, cudaStream_t stream) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if ((e = prepare(dev)) != cudaSuccess) return e;
-    CUtensorMap map;
-    if (!make_kv_map(&map, p.kcache, p.num_blocks)) return cudaErrorInvalidValue;
-    const int tiles = (p.rows + kTileRows - 1) / kTileRows;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * p.num_parts, tiles, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;  // prologue overlaps the previous kernel
-    attr.val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, split_kv_tc_kernel, map, p);
-}
-
+int split_kv_tc_tile_rows() { return kTileRows; }  // the same for every row width
 }  // namespace mla

@@ -68,7 +68,9 @@ UNIFORM = Case("uniform", batch=64, s_q=1, h_q=128, seqlens=(4096,) * 64, pool_p
 VARIABLE = Case("variable", batch=128, s_q=1, h_q=128, seqlen_range=(256, 16384), seed=2)
 MTP = Case("mtp", batch=32, s_q=8, h_q=128, seqlens=(8192,) * 32, causal=True, seed=3)
 LONG = Case("long", batch=64, s_q=1, h_q=128, seqlens=(65536,) * 64, seed=4)
-CASES = {c.name: c for c in (TINY, UNIFORM, VARIABLE, MTP, LONG)}
+# the d_qk = 512 variant: a 512-wide cached row that is both key and value
+UNIFORM_D512 = Case("uniform_d512", batch=64, s_q=1, h_q=128, seqlens=(4096,) * 64, pool_pages=4096, seed=5, d=512)
+CASES = {c.name: c for c in (TINY, UNIFORM, VARIABLE, MTP, LONG, UNIFORM_D512)}
 
 
 @dataclasses.dataclass

@@ -110,6 +110,7 @@ def pin_brute_force(decode, seed=11):
         (3, 1, 4, 1, [1, 64, 200], False, 576, 512, 64),
         (2, 3, 4, 1, [5, 130], True, 576, 512, 64),
         (2, 2, 4, 2, [70, 3], False, 576, 512, 64),
+        (2, 2, 8, 1, [130, 65], True, 512, 512, 64),    # the 512-wide row: V is the whole row
         (1, 4, 2, 1, [9], True, 40, 24, 4),
     ]
     for (b, s_q, h_q, h_kv, seqlens, causal, d, dv, page) in cases:

@@ -84,7 +84,8 @@ def _decode(lib, **over):
     (dict(batch=0), _lib.MLA_ERR_INVALID_ARG),
     (dict(num_parts=0), _lib.MLA_ERR_INVALID_ARG),
     (dict(scale=float("nan")), _lib.MLA_ERR_INVALID_ARG),
-    (dict(d=512), _lib.MLA_ERR_UNSUPPORTED),
+    (dict(d=500), _lib.MLA_ERR_UNSUPPORTED),          # row widths: 576 and 512 only
+    (dict(d=448), _lib.MLA_ERR_UNSUPPORTED),
     (dict(dv=256), _lib.MLA_ERR_UNSUPPORTED),
     (dict(h_kv=2, h_q=16), _lib.MLA_ERR_UNSUPPORTED),
     (dict(s_q=1024, h_q=128), _lib.MLA_ERR_UNSUPPORTED),

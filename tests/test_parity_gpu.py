@@ -196,6 +196,16 @@ def test_graph_capture_matches_eager():
     assert torch.equal(o, o_e) and torch.equal(lse, l_e)
 
 
+@pytest.mark.parametrize("batch,s_q,h_q,seqlens,causal", [(3, 1, 128, [300, 1000, 77], False),
+                                                        (2, 4, 64, [500, 130], True),
+                                                        (2, 1, 16, [0, 65], False)])
+def test_row_width_512(batch, s_q, h_q, seqlens, causal):
+    # the 512-wide cached row (no RoPE part): eight 64-dim chunks per page
+    c = dataclasses.replace(case("d512", batch, s_q, h_q, seqlens, causal=causal, seed=117), d=512)
+    for parts in (None, 2):
+        check(c, num_parts=parts)
+
+
 def test_deterministic():
     c = case("det", 2, 1, 128, [2000, 900], seed=110)
     x = to_device(W.make_inputs(c, "cpu"), DEV)
@@ -217,7 +227,7 @@ def test_empty_segments_between_full_ones():
             assert torch.equal(o, o2) and torch.equal(lse, l2), parts
 
 
-@pytest.mark.parametrize("name", ["uniform", "variable", "mtp", "long"])
+@pytest.mark.parametrize("name", ["uniform", "variable", "mtp", "long", "uniform_d512"])
 def test_full_size_repeatable(name):
     # bit-identical outputs over repeated launches at full size: every wait
     # on the hand-offs between the two CTAs of a pair has to be exact
@@ -234,7 +244,7 @@ def test_full_size_repeatable(name):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("name", ["uniform", "variable", "mtp", "long"])
+@pytest.mark.parametrize("name", ["uniform", "variable", "mtp", "long", "uniform_d512"])
 def test_full_size_sampled(name):
     c = W.CASES[name]
     x = W.make_inputs(c, device="cuda")
