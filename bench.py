@@ -49,6 +49,13 @@ METRIC = "MLA decode µs/call, KV-cache GB/s and TFLOPS vs GB300 roofline"
 
 
 # ------------------------------------------------------------------ workload figures
+def workload_label(case):
+    """The workload named by what it is, with its sizes (the same string in both arms)."""
+    lengths = "U" + str(case.seqlen_range) if case.seqlen_range else case.seqlens[0]
+    return (f"{case.name}: b={case.batch}, s_q={case.s_q}, h_q={case.h_q}, h_kv={case.h_kv}, d={case.d}, "
+            f"dv={case.dv}, page={case.page}, causal={case.causal}, seqlens={lengths}")
+
+
 def workload_figures(case, seqlens):
     """Algorithmic bytes and FLOPs of one decode call."""
     from mla_decode_attention_latent_gb300 import workloads as W
@@ -361,9 +368,7 @@ def main():
             "hbm_frac_of_" + pk["source"]: round(value / pk["hbm_gbs"], 4),
             "hbm_frac_of_nominal_8tbs": round(value / 8000.0, 4),
             "tensor_frac_of_" + pk["source"]: round(tflops / pk["bf16_tflops"], 4),
-            "config": {"workload": f"{case.name}: b={case.batch}, s_q={case.s_q}, h_q={case.h_q}, h_kv={case.h_kv}, "
-                                   f"d={case.d}, dv={case.dv}, page={case.page}, causal={case.causal}, "
-                                   f"seqlens={'U' + str(case.seqlen_range) if case.seqlen_range else case.seqlens[0]}",
+            "config": {"workload": workload_label(case),
                        "batch": case.batch, "s_q": case.s_q, "h_q": case.h_q, "num_parts": num_parts,
                        "kv_bytes": fig["kv_bytes"], "bytes_per_call": fig["bytes"], "flops_per_call": fig["flops"],
                        "l2": "no flush: KV pages touched per call exceed the 129 MB L2",
@@ -444,7 +449,9 @@ def reference_arm(args, case):
     line = {"metric": METRIC, "impl": "reference", "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(call * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": case.name, "batch": case.batch, "s_q": case.s_q, "h_q": case.h_q},
+            "config": {"workload": workload_label(case), "batch": case.batch, "s_q": case.s_q, "h_q": case.h_q,
+                       "kv_bytes": fig["kv_bytes"], "bytes_per_call": fig["bytes"], "flops_per_call": fig["flops"],
+                       "parallelism": "host cores, rank 0 only"},
             "cpu_baseline": {"kind": "oracle", "cores": cores, "value": round(value, 4), "unit": "GB/s",
                              "sample": f"{seqs} of {case.batch} sequences per step, scaled to one call"},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
