@@ -166,6 +166,13 @@ MLA_API size_t mla_workspace_bytes(int batch, int s_q, int h_q, int h_kv, int dv
  *                  256-byte aligned; its contents on entry do not matter
  * Out-of-range block ids or lengths found on the device are skipped and set
  * bits in the device status word (mla_device_status); they never fault.
+ * Stream order: two kernels are enqueued on `stream` (split-KV, then the
+ * combine), both as programmatic dependent launches.  Each may be scheduled
+ * while the kernel before it is finishing, but reads and writes no global
+ * memory until that kernel has completed, so the call observes every earlier
+ * write on the stream exactly as an ordinary launch would.  The launches can
+ * be captured in a CUDA graph once the first call on a device has set the
+ * kernel attributes.
  * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_WORKSPACE,
  *         MLA_ERR_CUDA (launch failure).
  */
