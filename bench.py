@@ -91,6 +91,16 @@ def peaks():
             "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def roofline(fig, kernel_ms, pk):
+    """(bound, achieved, peak, unit) of one launch: the roof that binds is picked
+    by the workload's FLOPs per byte against the ridge point of the two peaks
+    (h_q = 128 decode sits just below it; multi-token decode far above)."""
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if fig["flops"] / fig["bytes"] > ridge:
+        return "tensor", fig["flops"] / (kernel_ms * 1e-3) / 1e12, pk["bf16_tflops"], "TFLOP/s"
+    return "hbm", fig["bytes"] / (kernel_ms * 1e-3) / 1e9, pk["hbm_gbs"], "GB/s"
+
+
 def split_kernel_traffic(workload):
     """DRAM bytes per split-KV launch from the committed ncu summary, if the kernel is unchanged since."""
     path = os.path.join(ROOT, "profiles", f"split_kv_{workload}.md")
@@ -333,15 +343,7 @@ def main():
     value = aggregate_gbs(fig["bytes"], world, ms_step)
     tflops = fig["flops"] * world / (ms_step * 1e-3) / 1e12
     pk = peaks()
-    # the roof that binds: the workload's FLOPs per byte against the ridge
-    # point of the two measured peaks (h_q = 128 decode sits just below it;
-    # multi-token decode far above)
-    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
-    bound = "tensor" if fig["flops"] / fig["bytes"] > ridge else "hbm"
-    if bound == "tensor":
-        achieved, peak, unit = fig["flops"] / (split_ms * 1e-3) / 1e12, pk["bf16_tflops"], "TFLOP/s"
-    else:
-        achieved, peak, unit = fig["bytes"] / (split_ms * 1e-3) / 1e9, pk["hbm_gbs"], "GB/s"
+    bound, achieved, peak, unit = roofline(fig, split_ms, pk)
     traffic = split_kernel_traffic(args.workload)
 
     # end-to-end through the public API with host buffers
