@@ -18,6 +18,12 @@ in this order):
   4. ``kcache``: fp32 N(0, 1), rounded to bf16.  Rows past a sequence's end in
      its last page, and pool pages no sequence uses, hold the same finite
      random values (callers may overwrite them to test robustness).
+     e4m3 cases (``fp8``) quantize the same fp32 draws per token instead:
+     scale_j = max_c |k_j[c]| / 448 (1 for an all-zero row), codes = k_j /
+     scale_j clamped to [-448, 448] and rounded to e4m3 (torch's cast, round
+     to nearest even), packed per page as 64 rows of codes then the 64 fp32
+     scales (``MLA_FP8_PAGE_BYTES``).  This is how a cache in that format can
+     be filled; the decode itself only ever dequantizes.
 
 Shapes follow the DeepSeek-style latent cache of the usage page ("FlashMLA란
 무엇인가?", sections "FlashMLA의 주요 특성" and "FlashMLA 설치 및 사용"):
@@ -52,6 +58,12 @@ class Case:
     page: int = PAGE
     pool_pages: Optional[int] = None             # physical pages; default = pages needed
     seed: int = 0
+    fp8: bool = False                            # packed e4m3 pages with per-token scales
+
+    @property
+    def page_bytes(self) -> int:
+        """Bytes of one cache page: bf16 rows, or e4m3 codes + fp32 scales."""
+        return self.page * self.d + self.page * 4 if self.fp8 else self.page * self.h_kv * self.d * 2
 
     @property
     def softmax_scale(self) -> float:
@@ -70,14 +82,16 @@ MTP = Case("mtp", batch=32, s_q=8, h_q=128, seqlens=(8192,) * 32, causal=True, s
 LONG = Case("long", batch=64, s_q=1, h_q=128, seqlens=(65536,) * 64, seed=4)
 # the d_qk = 512 variant: a 512-wide cached row that is both key and value
 UNIFORM_D512 = Case("uniform_d512", batch=64, s_q=1, h_q=128, seqlens=(4096,) * 64, pool_pages=4096, seed=5, d=512)
-CASES = {c.name: c for c in (TINY, UNIFORM, VARIABLE, MTP, LONG, UNIFORM_D512)}
+# the uniform decode over an e4m3 cache with per-token scales
+UNIFORM_FP8 = Case("uniform_fp8", batch=64, s_q=1, h_q=128, seqlens=(4096,) * 64, pool_pages=4096, seed=6, fp8=True)
+CASES = {c.name: c for c in (TINY, UNIFORM, VARIABLE, MTP, LONG, UNIFORM_D512, UNIFORM_FP8)}
 
 
 @dataclasses.dataclass
 class Inputs:
     case: Case
     q: torch.Tensor              # [b, s_q, h_q, d] bf16
-    kcache: torch.Tensor         # [num_blocks, page, h_kv, d] bf16
+    kcache: torch.Tensor         # [num_blocks, page, h_kv, d] bf16, or uint8 [num_blocks, page_bytes] (fp8)
     block_table: torch.Tensor    # [b, max_blocks] int32
     cache_seqlens: torch.Tensor  # [b] int32
 
@@ -126,14 +140,46 @@ def make_inputs(case: Case, device: str = "cpu", seqlens: Optional[Sequence[int]
         dgen.manual_seed(case.seed + 1_000_003)
     q = torch.randn((case.batch, case.s_q, case.h_q, case.d), generator=dgen, device=device,
                     dtype=torch.float32).to(torch.bfloat16)
-    kcache = torch.empty((pool, case.page, case.h_kv, case.d), dtype=torch.bfloat16, device=device)
+    if case.fp8:
+        if case.h_kv != 1:
+            raise ValueError("packed e4m3 pages hold one KV head")
+        kcache = torch.empty((pool, case.page_bytes), dtype=torch.uint8, device=device)
+    else:
+        kcache = torch.empty((pool, case.page, case.h_kv, case.d), dtype=torch.bfloat16, device=device)
     # draw the pool in slabs to bound the fp32 temporary
     slab = max(1, (1 << 27) // (case.page * case.h_kv * case.d))
     for s in range(0, pool, slab):
         e = min(pool, s + slab)
-        kcache[s:e] = torch.randn((e - s, case.page, case.h_kv, case.d), generator=dgen, device=device,
-                                  dtype=torch.float32).to(torch.bfloat16)
+        x = torch.randn((e - s, case.page, case.h_kv, case.d), generator=dgen, device=device, dtype=torch.float32)
+        if case.fp8:
+            kcache[s:e] = pack_e4m3_pages(x[:, :, 0, :])
+        else:
+            kcache[s:e] = x.to(torch.bfloat16)
     return Inputs(case, q, kcache, bt.to(device), sl.to(device))
+
+
+def pack_e4m3_pages(rows: torch.Tensor, scales: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Quantize fp32 rows [n, page, d] per token and pack them as uint8 pages
+    [n, page * d + page * 4] (codes, then fp32 scales).  ``scales`` [n, page]
+    overrides the per-token max-abs / 448 choice."""
+    n, page, d = rows.shape
+    if scales is None:
+        amax = rows.abs().amax(dim=-1)
+        scales = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    scales = scales.to(torch.float32)
+    codes = (rows / scales[..., None]).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+    out = torch.empty((n, page * d + page * 4), dtype=torch.uint8, device=rows.device)
+    out[:, :page * d] = codes.view(torch.uint8).reshape(n, page * d)
+    out[:, page * d:] = scales.contiguous().view(torch.uint8).reshape(n, page * 4)
+    return out
+
+
+def e4m3_page_codes(pages: torch.Tensor, d: int = D_QK, page: int = PAGE):
+    """Views of packed pages: (codes uint8 [n, page, d], scales fp32 [n, page])."""
+    n = pages.shape[0]
+    codes = pages[:, :page * d].reshape(n, page, d)
+    scales = pages[:, page * d:].contiguous().view(torch.float32).reshape(n, page)
+    return codes, scales
 
 
 def kv_pages_touched(cache_seqlens, page: int = PAGE) -> int:

@@ -9,6 +9,8 @@ method's arithmetic.
 
 Contents
   ``mla_decode``   the decode definition in fp64 (plain C, ``mla_oracle.c``)
+  ``mla_decode_fp8``  the same over packed e4m3 pages with per-token scales
+  ``e4m3_to_float64``  the OCP e4m3 decoding the fp8 path uses
   ``schedule``     the split-KV work partition restated in plain Python
                    (``schedule.py``)
 
@@ -59,6 +61,10 @@ def load_library(path: str):
         ctypes.c_double, ctypes.c_int, ctypes.c_void_p, ctypes.c_int64,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
     ]
+    lib.oracle_mla_decode_fp8.restype = ctypes.c_int
+    lib.oracle_mla_decode_fp8.argtypes = lib.oracle_mla_decode.argtypes
+    lib.oracle_e4m3_to_double.restype = ctypes.c_double
+    lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
     lib.oracle_max_threads.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
     return lib
@@ -82,6 +88,58 @@ def _bits(a: np.ndarray) -> np.ndarray:
     if a.dtype != np.uint16:
         raise TypeError("bf16 inputs are passed as their uint16 bit patterns")
     return a
+
+
+def e4m3_to_float64(codes, lib=None) -> np.ndarray:
+    """fp64 values of OCP e4m3 codes (uint8 array), decoded by ``mla_oracle.c``."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    f = (lib or _load()).oracle_e4m3_to_double
+    return np.array([f(int(c)) for c in codes.reshape(-1)], dtype=np.float64).reshape(codes.shape)
+
+
+def _outputs(q, bt, sl, dv, rows):
+    """Check the table shapes; allocate (o, lse, rows array or None, row count)."""
+    b, s_q, h_q, d = q.shape
+    if bt.ndim != 2 or bt.shape[0] != b or sl.shape != (b,):
+        raise ValueError("block_table must be [b, max_blocks] and cache_seqlens [b]")
+    if rows is None:
+        n_rows = b * s_q * h_q
+        rows_arr = None
+        o = np.zeros((b, s_q, h_q, dv), dtype=np.float64)
+        lse = np.zeros((b, s_q, h_q), dtype=np.float64)
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+        n_rows = rows_arr.shape[0]
+        o = np.zeros((n_rows, dv), dtype=np.float64)
+        lse = np.zeros((n_rows,), dtype=np.float64)
+    return o, lse, rows_arr, n_rows
+
+
+def mla_decode_fp8(q_bits, kv_pages, block_table, cache_seqlens, dv, softmax_scale,
+                   causal=False, rows=None, nthreads=0, lib=None):
+    """fp64 MLA decode over packed e4m3 pages (see ``mla_oracle.c``).
+
+    kv_pages  uint8 [num_blocks, 64 * d + 256]: per page 64 rows of d e4m3
+              codes, then 64 little-endian fp32 scales; row j is scale_j * code_j
+    Other arguments and the result as ``mla_decode`` (one KV head).
+    """
+    q = _bits(q_bits)
+    kv = np.ascontiguousarray(kv_pages, dtype=np.uint8)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(cache_seqlens, dtype=np.int32)
+    b, s_q, h_q, d = q.shape
+    page = 64
+    if kv.ndim != 2 or kv.shape[1] != page * d + page * 4:
+        raise ValueError(f"kv_pages must be [num_blocks, {page * d + page * 4}] for d = {d}")
+    o, lse, rows_arr, n_rows = _outputs(q, bt, sl, dv, rows)
+    st = (lib or _load()).oracle_mla_decode_fp8(
+        q.ctypes.data, kv.ctypes.data, kv.shape[0], page, bt.ctypes.data, bt.shape[1],
+        sl.ctypes.data, b, s_q, h_q, 1, d, dv, float(softmax_scale), int(bool(causal)),
+        None if rows_arr is None else rows_arr.ctypes.data, n_rows,
+        o.ctypes.data, lse.ctypes.data, int(nthreads))
+    if st != 0:
+        raise ValueError(f"oracle_mla_decode_fp8 failed with status {st}")
+    return o, lse
 
 
 def mla_decode(q_bits, kcache_bits, block_table, cache_seqlens, dv, softmax_scale,

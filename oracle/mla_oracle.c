@@ -34,6 +34,18 @@
  *
  * Inputs arrive as raw bf16 bit patterns (uint16) and are widened to double
  * exactly; all arithmetic is fp64.
+ *
+ * The cache may instead be packed e4m3 pages with per-token scales
+ * (oracle_mla_decode_fp8).  The page "[flashinfer] FlashInfer, SM120 GPU를
+ * 위한 희소 MLA 커널 추가로 LLM 추론 속도 향상" (item 5) names a packed KV cache
+ * whose scale format is a parameter, and "[vllm] Blackwell을 위한 새로운 MLA
+ * 백엔드: TOKENSPEED_MLA 분석" (section "들어가며") an FP8 KV cache; neither gives
+ * a layout.  The reading taken: a page is 64 rows of d e4m3 codes followed by
+ * 64 little-endian fp32 scales, and row j is k_j[c] = scale_j * e4m3(code_jc),
+ * formed exactly in fp64; the attention above is then applied to these rows
+ * unchanged.  e4m3 is the OCP 8-bit float E4M3: sign bit, 4 exponent bits with
+ * bias 7, 3 mantissa bits; exponent 0 encodes subnormals m/8 * 2^-6; S.1111.111
+ * is NaN; there are no infinities (largest finite value 448).
  */
 #include <math.h>
 #include <stdint.h>
@@ -56,12 +68,42 @@ static double bf16_bits_to_double(uint16_t bits) {
     return (double)f;
 }
 
+/* One OCP e4m3 code as a double (definition in the header comment). */
+double oracle_e4m3_to_double(uint8_t code) {
+    int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);        /* m/8 * 2^(1-7) */
+    else v = ldexp((double)(8 + m), e - 10);     /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* Where cached rows come from: bf16 rows, or packed e4m3 pages. */
+typedef struct {
+    const uint16_t *bf16;   /* [num_blocks][page][h_kv][d] bf16 bits, or NULL */
+    const uint8_t *e4m3;    /* [num_blocks][page * d + page * 4] packed pages (h_kv = 1), or NULL */
+} cache_view;
+
+/* Cached row `t` of page `blk`, KV head g, as d doubles (exact). */
+static void load_row(const cache_view *cv, int64_t blk, int page, int64_t t, int h_kv, int64_t g, int d,
+                     double *row) {
+    if (cv->bf16) {
+        const uint16_t *krow = cv->bf16 + ((blk * page + t) * h_kv + g) * (int64_t)d;
+        for (int c = 0; c < d; ++c) row[c] = bf16_bits_to_double(krow[c]);
+    } else {
+        const uint8_t *pg = cv->e4m3 + blk * ((int64_t)page * d + (int64_t)page * 4);
+        float sc;
+        memcpy(&sc, pg + (int64_t)page * d + 4 * t, sizeof sc);
+        for (int c = 0; c < d; ++c) row[c] = (double)sc * oracle_e4m3_to_double(pg[t * d + c]);
+    }
+}
+
 /* One output row: flat row index r = (b * s_q + i) * h_q + h. */
-static int oracle_one_row(const uint16_t *q, const uint16_t *kcache, int64_t num_blocks,
+static int oracle_one_row(const uint16_t *q, const cache_view *cv, int64_t num_blocks,
                           int page, const int32_t *block_table, int max_blocks,
                           const int32_t *cache_seqlens, int s_q, int h_q, int h_kv, int d,
                           int dv, double scale, int causal, int64_t r, double *o_row,
-                          double *lse_row, double *scores) {
+                          double *lse_row, double *scores, double *krow) {
     int64_t h = r % h_q;
     int64_t i = (r / h_q) % s_q;
     int64_t b = r / ((int64_t)h_q * s_q);
@@ -80,9 +122,9 @@ static int oracle_one_row(const uint16_t *q, const uint16_t *kcache, int64_t num
     for (int64_t j = 0; j < T; ++j) {
         int64_t blk = block_table[b * max_blocks + j / page];
         if (blk < 0 || blk >= num_blocks) return ORACLE_ERR_BLOCK;
-        const uint16_t *krow = kcache + ((blk * page + j % page) * h_kv + g) * (int64_t)d;
+        load_row(cv, blk, page, j % page, h_kv, g, d, krow);
         double acc = 0.0;
-        for (int c = 0; c < d; ++c) acc += bf16_bits_to_double(qrow[c]) * bf16_bits_to_double(krow[c]);
+        for (int c = 0; c < d; ++c) acc += bf16_bits_to_double(qrow[c]) * krow[c];
         scores[j] = scale * acc;
     }
 
@@ -98,30 +140,19 @@ static int oracle_one_row(const uint16_t *q, const uint16_t *kcache, int64_t num
     /* O = sum_j softmax_j * V_j, V_j = first dv dims of the cached row */
     for (int64_t j = 0; j < T; ++j) {
         int64_t blk = block_table[b * max_blocks + j / page];
-        const uint16_t *krow = kcache + ((blk * page + j % page) * h_kv + g) * (int64_t)d;
+        load_row(cv, blk, page, j % page, h_kv, g, d, krow);
         double w = exp(scores[j] - lse);
-        for (int v = 0; v < dv; ++v) o_row[v] += w * bf16_bits_to_double(krow[v]);
+        for (int v = 0; v < dv; ++v) o_row[v] += w * krow[v];
     }
     return ORACLE_OK;
 }
 
-/*
- * Compute the requested rows.
- *   q            [batch, s_q, h_q, d]            bf16 bits
- *   kcache       [num_blocks, page, h_kv, d]     bf16 bits
- *   block_table  [batch, max_blocks]             int32 physical page ids
- *   cache_seqlens[batch]                         int32
- *   rows         n_rows flat row ids (b*s_q+i)*h_q+h, or NULL for all rows
- *   o            [n_rows, dv] fp64 out;  lse [n_rows] fp64 out
- *   nthreads     OpenMP threads (<= 0: runtime default)
- * Returns 0, or a negative error (bad argument, page id out of range, no memory).
- */
-int oracle_mla_decode(const uint16_t *q, const uint16_t *kcache, int64_t num_blocks, int page,
-                      const int32_t *block_table, int max_blocks, const int32_t *cache_seqlens,
-                      int batch, int s_q, int h_q, int h_kv, int d, int dv, double scale,
-                      int causal, const int64_t *rows, int64_t n_rows, double *o, double *lse,
-                      int nthreads) {
-    if (!q || !kcache || !block_table || !cache_seqlens || !o || !lse) return ORACLE_ERR_ARG;
+static int decode_rows(const uint16_t *q, const cache_view *cv, int64_t num_blocks, int page,
+                       const int32_t *block_table, int max_blocks, const int32_t *cache_seqlens,
+                       int batch, int s_q, int h_q, int h_kv, int d, int dv, double scale,
+                       int causal, const int64_t *rows, int64_t n_rows, double *o, double *lse,
+                       int nthreads) {
+    if (!q || !block_table || !cache_seqlens || !o || !lse) return ORACLE_ERR_ARG;
     if (batch < 0 || s_q <= 0 || h_q <= 0 || h_kv <= 0 || h_q % h_kv || d <= 0 || dv <= 0 ||
         dv > d || page <= 0 || max_blocks < 0)
         return ORACLE_ERR_ARG;
@@ -143,7 +174,8 @@ int oracle_mla_decode(const uint16_t *q, const uint16_t *kcache, int64_t num_blo
 #endif
     {
         double *scores = (double *)malloc(sizeof(double) * (size_t)(max_T > 0 ? max_T : 1));
-        if (!scores) {
+        double *krow = (double *)malloc(sizeof(double) * (size_t)d);
+        if (!scores || !krow) {
 #ifdef _OPENMP
 #pragma omp atomic write
 #endif
@@ -153,11 +185,11 @@ int oracle_mla_decode(const uint16_t *q, const uint16_t *kcache, int64_t num_blo
 #pragma omp for schedule(dynamic, 1)
 #endif
         for (int64_t n = 0; n < n_rows; ++n) {
-            if (!scores) continue;
+            if (!scores || !krow) continue;
             int64_t r = rows ? rows[n] : n;
-            int st = oracle_one_row(q, kcache, num_blocks, page, block_table, max_blocks,
+            int st = oracle_one_row(q, cv, num_blocks, page, block_table, max_blocks,
                                     cache_seqlens, s_q, h_q, h_kv, d, dv, scale, causal, r,
-                                    o + n * (int64_t)dv, lse + n, scores);
+                                    o + n * (int64_t)dv, lse + n, scores, krow);
             if (st != ORACLE_OK) {
 #ifdef _OPENMP
 #pragma omp atomic write
@@ -166,8 +198,46 @@ int oracle_mla_decode(const uint16_t *q, const uint16_t *kcache, int64_t num_blo
             }
         }
         free(scores);
+        free(krow);
     }
     return status;
+}
+
+/*
+ * Compute the requested rows over a bf16 cache.
+ *   q            [batch, s_q, h_q, d]            bf16 bits
+ *   kcache       [num_blocks, page, h_kv, d]     bf16 bits
+ *   block_table  [batch, max_blocks]             int32 physical page ids
+ *   cache_seqlens[batch]                         int32
+ *   rows         n_rows flat row ids (b*s_q+i)*h_q+h, or NULL for all rows
+ *   o            [n_rows, dv] fp64 out;  lse [n_rows] fp64 out
+ *   nthreads     OpenMP threads (<= 0: runtime default)
+ * Returns 0, or a negative error (bad argument, page id out of range, no memory).
+ */
+int oracle_mla_decode(const uint16_t *q, const uint16_t *kcache, int64_t num_blocks, int page,
+                      const int32_t *block_table, int max_blocks, const int32_t *cache_seqlens,
+                      int batch, int s_q, int h_q, int h_kv, int d, int dv, double scale,
+                      int causal, const int64_t *rows, int64_t n_rows, double *o, double *lse,
+                      int nthreads) {
+    if (!kcache) return ORACLE_ERR_ARG;
+    cache_view cv = {kcache, NULL};
+    return decode_rows(q, &cv, num_blocks, page, block_table, max_blocks, cache_seqlens, batch, s_q, h_q,
+                       h_kv, d, dv, scale, causal, rows, n_rows, o, lse, nthreads);
+}
+
+/*
+ * The same over packed e4m3 pages: kv_pages [num_blocks][page * d + page * 4]
+ * bytes (codes, then fp32 scales), one KV head (h_kv must be 1).
+ */
+int oracle_mla_decode_fp8(const uint16_t *q, const uint8_t *kv_pages, int64_t num_blocks, int page,
+                          const int32_t *block_table, int max_blocks, const int32_t *cache_seqlens,
+                          int batch, int s_q, int h_q, int h_kv, int d, int dv, double scale,
+                          int causal, const int64_t *rows, int64_t n_rows, double *o, double *lse,
+                          int nthreads) {
+    if (!kv_pages || h_kv != 1) return ORACLE_ERR_ARG;
+    cache_view cv = {NULL, kv_pages};
+    return decode_rows(q, &cv, num_blocks, page, block_table, max_blocks, cache_seqlens, batch, s_q, h_q,
+                       h_kv, d, dv, scale, causal, rows, n_rows, o, lse, nthreads);
 }
 
 /* Threads the oracle will use by default (for reporting the CPU baseline). */

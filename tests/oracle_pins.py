@@ -21,6 +21,17 @@ fact that the mathematics (or a page's worked definition) fixes:
   pin_saturated_softmax  one key's score exceeds the others by ~1000: O is that
                          key's V row and LSE its score (needs the max shift)
 
+Pins of the packed e4m3 cache (``FP8_PINS``; they take the bf16 decode, the
+e4m3 decode and the oracle's e4m3 code decoder):
+
+  pin_e4m3_codes         all 256 codes against torch's float8_e4m3fn decoding
+                         (a library routine) and the OCP E4M3 landmarks
+  pin_fp8_matches_bf16   with power-of-two scales every dequantized value is a
+                         bf16 value: the e4m3 decode must then equal, bit for
+                         bit, the bf16 decode of the dequantized cache
+  pin_fp8_scale_linearity  doubling every token's scale and halving q leaves
+                         the scores unchanged and doubles O exactly
+
 The mutation test in ``test_oracle_pins.py`` plants mistakes in a copy of the
 oracle's C source and checks that some pin catches each one.
 """
@@ -298,3 +309,105 @@ def pin_saturated_softmax(decode, seed=20):
 ALL_PINS = [pin_brute_force, pin_permutation, pin_q_zero, pin_seqlen_one, pin_two_key_golden,
             pin_score_shift, pin_causal_consistency, pin_zero_visible, pin_kv_head_groups,
             pin_sampled_rows, pin_saturated_softmax]
+
+
+# ---------------------------------------------------------------- e4m3 cache pins
+E4M3_NAN_CODES = (0x7F, 0xFF)
+
+
+def e4m3_codes_of(x) -> np.ndarray:
+    """Round values to e4m3 codes (torch's cast, nearest even) after clamping to +-448."""
+    t = torch.as_tensor(np.asarray(x, dtype=np.float32)).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+    return t.view(torch.uint8).numpy().copy()
+
+
+def e4m3_values_of(codes) -> np.ndarray:
+    """fp64 values of e4m3 codes through torch's own decoding."""
+    return torch.from_numpy(np.ascontiguousarray(codes, dtype=np.uint8)).view(torch.float8_e4m3fn).to(
+        torch.float64).numpy()
+
+
+def fp8_pages(codes, scales) -> np.ndarray:
+    """Pack codes uint8 [n, page, d] and scales fp32 [n, page] into [n, page * d + page * 4]."""
+    n, page, d = codes.shape
+    out = np.empty((n, page * d + page * 4), dtype=np.uint8)
+    out[:, :page * d] = codes.reshape(n, page * d)
+    out[:, page * d:] = np.ascontiguousarray(scales, dtype="<f4").view(np.uint8).reshape(n, page * 4)
+    return out
+
+
+def _fp8_case(rng, seqlens, d, page, pow2_scales):
+    """Random e4m3 cache for `seqlens`: (pages, dequantized fp64 [pool, page, d], block_table).
+
+    Rows past each sequence's end and unused pages hold random codes (NaN codes
+    included) and NaN scales: no decode may read them."""
+    n_pages = [(T + page - 1) // page for T in seqlens]
+    pool = sum(n_pages) + 2
+    codes = e4m3_codes_of(rng.standard_normal((pool, page, d)) * 8.0)
+    if pow2_scales:
+        scales = np.exp2(rng.integers(-5, 0, size=(pool, page))).astype(np.float32)
+    else:
+        scales = rng.uniform(0.01, 0.2, size=(pool, page)).astype(np.float32)
+    used = np.zeros((pool, page), dtype=bool)
+    perm = rng.permutation(pool).astype(np.int32)
+    bt = np.zeros((len(seqlens), max(n_pages)), dtype=np.int32)
+    cur = 0
+    for b, T in enumerate(seqlens):
+        for p in range(n_pages[b]):
+            bt[b, p] = perm[cur]
+            used[perm[cur], :min(page, T - p * page)] = True
+            cur += 1
+    junk = rng.integers(0, 256, size=codes.shape).astype(np.uint8)
+    junk[..., :2] = E4M3_NAN_CODES
+    codes = np.where(used[..., None], codes, junk)
+    scales = np.where(used, scales, np.float32(np.nan)).astype(np.float32)
+    deq = e4m3_values_of(codes) * scales[..., None].astype(np.float64)
+    return fp8_pages(codes, scales), deq, used, bt
+
+
+def pin_e4m3_codes(decode, decode_fp8, e4m3):
+    codes = np.arange(256, dtype=np.uint8)
+    v = e4m3(codes)
+    t = e4m3_values_of(codes)
+    assert np.array_equal(np.isnan(v), np.isnan(t)), "NaN codes differ from torch's e4m3"
+    assert np.array_equal(v[~np.isnan(v)], t[~np.isnan(t)]), "e4m3 values differ from torch's"
+    assert v[0x38] == 1.0 and v[0x7E] == 448.0 and v[0xFE] == -448.0, "e4m3 normal landmarks"
+    assert v[0x01] == 2.0 ** -9 and v[0x07] == 7 * 2.0 ** -9 and v[0x08] == 2.0 ** -6, "e4m3 subnormal landmarks"
+    assert np.isnan(v).sum() == 2 and all(np.isnan(v[c]) for c in E4M3_NAN_CODES), "e4m3 has exactly two NaNs"
+    assert v[0x80] == 0.0 and math.copysign(1.0, v[0x80]) == -1.0, "0x80 is -0"
+
+
+def pin_fp8_matches_bf16(decode, decode_fp8, e4m3, seed=21):
+    rng = np.random.default_rng(seed)
+    d, dv, page = 576, 512, 64
+    for seqlens, s_q, h_q, causal in (([130, 64, 7], 2, 8, True), ([1, 200], 1, 16, False)):
+        pages, deq, used, bt = _fp8_case(rng, seqlens, d, page, pow2_scales=True)
+        # the same rows as a bf16 cache: every dequantized value is a bf16 value
+        kc = bf16_bits_of(np.where(used[..., None], deq, 1e4 * rng.standard_normal(deq.shape)))[:, :, None, :]
+        assert np.array_equal(f64_of(kc[:, :, 0, :])[used], deq[used]), "dequantized rows must be bf16-exact"
+        q = rand_bits(rng, (len(seqlens), s_q, h_q, d))
+        sl = np.array(seqlens, np.int32)
+        o8, l8 = decode_fp8(q, pages, bt, sl, dv, 1.0 / 24, causal)
+        o, l = decode(q, kc, bt, sl, dv, 1.0 / 24, causal)
+        assert np.array_equal(l8, l), "e4m3 LSE differs from the bf16 decode of the same rows"
+        assert np.array_equal(o8, o), "e4m3 O differs from the bf16 decode of the same rows"
+
+
+def pin_fp8_scale_linearity(decode, decode_fp8, e4m3, seed=22):
+    rng = np.random.default_rng(seed)
+    d, dv, page = 576, 512, 64
+    seqlens = [100, 65]
+    pages, deq, used, bt = _fp8_case(rng, seqlens, d, page, pow2_scales=False)
+    q = rand_bits(rng, (2, 1, 16, d))
+    sl = np.array(seqlens, np.int32)
+    o1, l1 = decode_fp8(q, pages, bt, sl, dv, 1.0 / 24, False)
+    doubled = pages.copy()
+    sc = doubled[:, page * d:].view("<f4")
+    sc *= 2.0
+    q_half = bf16_bits_of(f64_of(q) / 2.0)
+    o2, l2 = decode_fp8(q_half, doubled, bt, sl, dv, 1.0 / 24, False)
+    assert np.array_equal(l2, l1), "scores must not change when q halves and the scales double"
+    assert np.array_equal(o2, 2.0 * o1), "O must double with the scales"
+
+
+FP8_PINS = [pin_e4m3_codes, pin_fp8_matches_bf16, pin_fp8_scale_linearity]

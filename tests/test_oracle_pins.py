@@ -20,26 +20,41 @@ def test_oracle_pin(pin):
     pin(oracle.mla_decode)
 
 
+@pytest.mark.parametrize("pin", pins.FP8_PINS, ids=lambda p: p.__name__)
+def test_oracle_fp8_pin(pin):
+    pin(oracle.mla_decode, oracle.mla_decode_fp8, oracle.e4m3_to_float64)
+
+
 # (description, text in mla_oracle.c, replacement)
 MUTANTS = [
     ("scale dropped", "scores[j] = scale * acc;", "scores[j] = acc;"),
     ("RoPE dims dropped", "for (int c = 0; c < d; ++c) acc +=", "for (int c = 0; c < dv; ++c) acc +="),
-    ("V read from the wrong dims", "o_row[v] += w * bf16_bits_to_double(krow[v]);",
-     "o_row[v] += w * bf16_bits_to_double(krow[v + (d - dv)]);"),
+    ("V read from the wrong dims", "o_row[v] += w * krow[v];", "o_row[v] += w * krow[v + (d - dv)];"),
     ("max missing from LSE", "double lse = M + log(sum);", "double lse = log(sum);"),
     ("causal window off by one", "if (causal) T = T - s_q + i + 1;", "if (causal) T = T - s_q + i;"),
-    ("in-page position taken as page", "+ j % page) * h_kv", "+ (j + 1) % page) * h_kv"),
+    ("in-page position taken as page", "cv->bf16 + ((blk * page + t) * h_kv", "cv->bf16 + ((blk * page + (t + 1) % page) * h_kv"),
     ("wrong KV head", "int64_t g = h / (h_q / h_kv);", "int64_t g = h % h_kv;"),
     ("weight sign flipped", "double w = exp(scores[j] - lse);", "double w = exp(lse - scores[j]);"),
     ("running max never updated", "for (int64_t j = 1; j < T; ++j)\n        if (scores[j] > M)",
      "for (int64_t j = 1; j < T; ++j)\n        if (scores[j] > M + 1e300)"),
+    # the e4m3 cache
+    ("e4m3 exponent bias", "ldexp((double)(8 + m), e - 10)", "ldexp((double)(8 + m), e - 11)"),
+    ("e4m3 subnormal step", "ldexp((double)m, -9)", "ldexp((double)m, -10)"),
+    ("scale of the neighbouring token", "+ 4 * t, sizeof sc)", "+ 4 * ((t + 1) % page), sizeof sc)"),
+    ("scale left out", "row[c] = (double)sc * oracle_e4m3_to_double(", "row[c] = oracle_e4m3_to_double("),
+    ("page stride without the scales", "blk * ((int64_t)page * d + (int64_t)page * 4)", "blk * ((int64_t)page * d)"),
 ]
 
 
-def _all_pins_pass(decode):
+def _all_pins_pass(decode, decode_fp8, e4m3):
     for pin in pins.ALL_PINS:
         try:
             pin(decode)
+        except (AssertionError, ValueError):
+            return False
+    for pin in pins.FP8_PINS:
+        try:
+            pin(decode, decode_fp8, e4m3)
         except (AssertionError, ValueError):
             return False
     return True
@@ -62,4 +77,10 @@ def test_pins_catch_planted_mistake(mutant):
         def decode(*args, **kw):
             return oracle.mla_decode(*args, lib=lib, **kw)
 
-        assert not _all_pins_pass(decode), f"no pin caught the planted mistake: {desc}"
+        def decode_fp8(*args, **kw):
+            return oracle.mla_decode_fp8(*args, lib=lib, **kw)
+
+        def e4m3(codes):
+            return oracle.e4m3_to_float64(codes, lib=lib)
+
+        assert not _all_pins_pass(decode, decode_fp8, e4m3), f"no pin caught the planted mistake: {desc}"
