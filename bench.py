@@ -52,14 +52,15 @@ METRIC = "MLA decode µs/call, KV-cache GB/s and TFLOPS vs GB300 roofline"
 def workload_label(case):
     """The workload named by what it is, with its sizes (the same string in both arms)."""
     lengths = "U" + str(case.seqlen_range) if case.seqlen_range else case.seqlens[0]
+    cache = ", cache=e4m3+per-token fp32 scales" if case.fp8 else ""
     return (f"{case.name}: b={case.batch}, s_q={case.s_q}, h_q={case.h_q}, h_kv={case.h_kv}, d={case.d}, "
-            f"dv={case.dv}, page={case.page}, causal={case.causal}, seqlens={lengths}")
+            f"dv={case.dv}, page={case.page}, causal={case.causal}, seqlens={lengths}{cache}")
 
 
 def workload_figures(case, seqlens):
     """Algorithmic bytes and FLOPs of one decode call."""
     from mla_decode_attention_latent_gb300 import workloads as W
-    page_bytes = case.page * case.h_kv * case.d * 2
+    page_bytes = case.page_bytes  # bf16 rows, or e4m3 codes + fp32 scales
     kv_bytes = W.kv_pages_touched(seqlens, case.page) * page_bytes
     q_bytes = case.batch * case.s_q * case.h_q * case.d * 2
     o_bytes = case.batch * case.s_q * case.h_q * case.dv * 2
@@ -70,7 +71,7 @@ def workload_figures(case, seqlens):
             keys += max(0, (t - case.s_q + i + 1) if case.causal else t)
     flops = 2.0 * case.h_q * (case.d + case.dv) * keys
     return {"bytes": kv_bytes + q_bytes + o_bytes + lse_bytes, "kv_bytes": kv_bytes, "flops": flops,
-            "valid_token_bytes": sum(seqlens) * case.h_kv * case.d * 2}
+            "valid_token_bytes": sum(seqlens) * page_bytes // case.page}
 
 
 def peaks():
@@ -235,13 +236,14 @@ def time_oracle(case, x_cpu, budget_s=10.0, max_seqs=None):
     R = case.s_q * case.h_q
     sl = x_cpu.cache_seqlens.numpy()
     q_bits = W.bf16_bits(x_cpu.q)
-    k_bits = W.bf16_bits(x_cpu.kcache)
+    k_data = x_cpu.kcache.numpy() if case.fp8 else W.bf16_bits(x_cpu.kcache)
+    decode = oracle.mla_decode_fp8 if case.fp8 else oracle.mla_decode
     bt = x_cpu.block_table.numpy()
 
     def run(seqs):
         rows = np.concatenate([np.arange(b * R, (b + 1) * R, dtype=np.int64) for b in seqs])
         t0 = time.perf_counter()
-        oracle.mla_decode(q_bits, k_bits, bt, sl, case.dv, case.softmax_scale, case.causal, rows=rows)
+        decode(q_bits, k_data, bt, sl, case.dv, case.softmax_scale, case.causal, rows=rows)
         return time.perf_counter() - t0
 
     t1 = run([0])
@@ -291,10 +293,12 @@ def main():
     ws = torch.empty((mla.mla_workspace_bytes(case.batch, case.s_q, case.h_q, case.h_kv, case.dv, num_parts),),
                      dtype=torch.uint8, device=dev)
 
+    decode = mla.mla_decode_kvcache_fp8 if case.fp8 else mla.mla_decode_kvcache
+
     def step():
         md_k, ns_k = mla.mla_get_metadata(x.cache_seqlens, case.num_q_rows, case.h_kv, num_parts=num_parts)
-        mla.mla_decode_kvcache(x.q, x.kcache, x.block_table, x.cache_seqlens, case.dv, md_k, ns_k,
-                               softmax_scale=case.softmax_scale, causal=case.causal, out=o, lse=lse, workspace=ws)
+        decode(x.q, x.kcache, x.block_table, x.cache_seqlens, case.dv, md_k, ns_k, softmax_scale=case.softmax_scale,
+               causal=case.causal, out=o, lse=lse, workspace=ws)
 
     for _ in range(args.warmup):
         step()
@@ -365,7 +369,7 @@ def main():
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f16" if case.fp8 else "bf16", "data": "synthetic",
             "us_per_call": round(ms_step * 1e3, 2), "tflops": round(tflops, 2),
             "hbm_frac_of_" + pk["source"]: round(value / pk["hbm_gbs"], 4),
             "hbm_frac_of_nominal_8tbs": round(value / 8000.0, 4),
@@ -400,6 +404,7 @@ def e2e_run(mla, case, x, fig, dev, stream, steps, world):
     hl = torch.empty((case.batch, case.s_q, case.h_q), dtype=torch.float32).pin_memory()
     dq, dk = torch.empty_like(x.q), torch.empty_like(x.kcache)
     dbt, dsl = torch.empty_like(x.block_table), torch.empty_like(x.cache_seqlens)
+    decode = mla.mla_decode_kvcache_fp8 if case.fp8 else mla.mla_decode_kvcache
 
     def one():
         dq.copy_(hq, non_blocking=True)
@@ -407,8 +412,7 @@ def e2e_run(mla, case, x, fig, dev, stream, steps, world):
         dbt.copy_(hbt, non_blocking=True)
         dsl.copy_(hsl, non_blocking=True)
         md, ns = mla.mla_get_metadata(dsl, case.num_q_rows, case.h_kv)
-        o, lse = mla.mla_decode_kvcache(dq, dk, dbt, dsl, case.dv, md, ns, softmax_scale=case.softmax_scale,
-                                        causal=case.causal)
+        o, lse = decode(dq, dk, dbt, dsl, case.dv, md, ns, softmax_scale=case.softmax_scale, causal=case.causal)
         ho.copy_(o, non_blocking=True)
         hl.copy_(lse, non_blocking=True)
 

@@ -36,7 +36,8 @@
  *  - bf16 tensors are raw IEEE bfloat16 bit patterns (2 bytes per element),
  *    row-major and densely packed in the shapes given.
  *
- * Supported on the GPU path: d = 576 or 512, dv = 512, page size 64,
+ * Supported on the GPU path: d = 576 or 512 (bf16 cache) or 576 (packed
+ * e4m3 cache, mla_decode_kvcache_fp8), dv = 512, page size 64,
  * h_kv = 1, any batch >= 1, any s_q >= 1 and h_q >= 1 with
  * s_q * h_q <= 65536.  d = 512 is the d_qk = 512 variant that the
  * "[FlashInfer] ... SM120 sparse MLA" page names for DSv4, read as a
@@ -183,6 +184,43 @@ MLA_API int mla_decode_kvcache(const void *q, const void *kcache, int64_t num_bl
                        const int32_t *num_splits, int num_parts, float softmax_scale,
                        int causal, void *o, float *lse, void *workspace,
                        size_t workspace_bytes, struct CUstream_st *stream);
+
+/*
+ * mla_decode_kvcache_fp8 — the same decode over a cache of packed e4m3 pages
+ * with per-token scales.
+ *
+ * The page "[flashinfer] FlashInfer, SM120 GPU를 위한 희소 MLA 커널 추가로 LLM
+ * 추론 속도 향상" (item 5, flashinfer/mla/trtllm.py) says that the MLA decode
+ * API takes a `kv_scale_format` for a packed KV cache with scales, and the page
+ * "[vllm] Blackwell을 위한 새로운 MLA 백엔드: TOKENSPEED_MLA 분석" (section
+ * "들어가며") runs the Blackwell decode on an FP8 KV cache; neither gives the
+ * layout.  This library's reading: a page of the cache is one packed
+ * record of MLA_FP8_PAGE_BYTES(d) bytes,
+ *   bytes [0, 64 d)          64 rows of d OCP e4m3 codes (row j, dim c at j d + c)
+ *   bytes [64 d, 64 d + 256) 64 fp32 per-token scales c_j (little endian)
+ * and cached row j dequantizes to k_j[c] = c_j * e4m3(code[j][c]).  The call
+ * then computes exactly what mla_decode_kvcache computes on the dequantized
+ * rows (V = their first 512 dims).
+ *
+ *   kv_pages       device bytes [num_blocks][MLA_FP8_PAGE_BYTES(d)]; 16-byte
+ *                  aligned.  Codes and scales of rows past a sequence's end
+ *                  may hold any bits.
+ *   d              576 only (other values: MLA_ERR_UNSUPPORTED)
+ *   everything else as for mla_decode_kvcache (q, o and lse stay bf16/fp32).
+ * Precision: the kernel computes in f16 on the tensor cores.  The e4m3 codes
+ * widen to f16 exactly; q is rounded to f16 (exact for |q| in [2^-17, 65504]);
+ * the softmax weights times c_j are rounded to f16, so |c_j| must stay below
+ * 255 (larger scales overflow; the call does not check the scales).
+ * Stream order, graph capture and errors: as for mla_decode_kvcache.
+ */
+#define MLA_FP8_PAGE_BYTES(d) (MLA_PAGE_SIZE * (d) + MLA_PAGE_SIZE * 4)
+MLA_API int mla_decode_kvcache_fp8(const void *q, const void *kv_pages, int64_t num_blocks,
+                                   const int32_t *block_table, int max_blocks_per_seq,
+                                   const int32_t *cache_seqlens, int batch, int s_q, int h_q, int h_kv,
+                                   int d, int dv, const int32_t *tile_scheduler_metadata,
+                                   const int32_t *num_splits, int num_parts, float softmax_scale,
+                                   int causal, void *o, float *lse, void *workspace,
+                                   size_t workspace_bytes, struct CUstream_st *stream);
 
 /*
  * mla_decode_kvcache_noalloc — mla_decode_kvcache for callers that cannot

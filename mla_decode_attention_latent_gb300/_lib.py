@@ -27,6 +27,11 @@ MLA_METADATA_INTS = 8
 
 MLA_NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024
 
+
+def MLA_FP8_PAGE_BYTES(d: int) -> int:
+    """Bytes of one packed e4m3 page: 64 rows of d codes, then 64 fp32 scales."""
+    return MLA_PAGE_SIZE * d + MLA_PAGE_SIZE * 4
+
 MLA_DEVERR_TIMEOUT = 0x1
 MLA_DEVERR_BLOCK_ID = 0x2
 MLA_DEVERR_SEQLEN = 0x4
@@ -39,6 +44,8 @@ SIGNATURES = {
     "mla_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "mla_decode_kvcache": (_I, [_P, _P, _I64, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _F, _I, _P, _P,
                                 _P, _SZ, _P]),
+    "mla_decode_kvcache_fp8": (_I, [_P, _P, _I64, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _F, _I, _P, _P,
+                                    _P, _SZ, _P]),
     "mla_decode_kvcache_noalloc": (_I, [_P, _P, _I64, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _F, _I, _P,
                                         _P, _P]),
     "mla_device_status": (_I, [ctypes.POINTER(ctypes.c_int), _I]),

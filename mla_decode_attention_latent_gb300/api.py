@@ -119,6 +119,60 @@ def mla_decode_kvcache(q: torch.Tensor, kcache: torch.Tensor, block_table: torch
     return out, lse
 
 
+def mla_decode_kvcache_fp8(q: torch.Tensor, kv_pages: torch.Tensor, block_table: torch.Tensor,
+                           cache_seqlens: torch.Tensor, dv: int, tile_scheduler_metadata: torch.Tensor,
+                           num_splits: torch.Tensor, softmax_scale: Optional[float] = None, causal: bool = False,
+                           out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                           workspace: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """MLA decode over packed e4m3 pages with per-token scales.
+
+    ``kv_pages`` is uint8 [num_blocks, MLA_FP8_PAGE_BYTES(d)]: per page, 64 rows
+    of d e4m3 codes, then 64 fp32 scales; row j dequantizes to scale_j * code_j
+    (layout and precision in ``include/mla_decode.h``).  Returns (o bf16
+    [b, s_q, h_q, dv], lse fp32 [b, s_q, h_q]) as ``mla_decode_kvcache``.
+    """
+    _need_cuda("q", q, torch.bfloat16)
+    _need_cuda("kv_pages", kv_pages, torch.uint8)
+    _need_cuda("block_table", block_table, torch.int32)
+    _need_cuda("cache_seqlens", cache_seqlens, torch.int32)
+    _need_cuda("tile_scheduler_metadata", tile_scheduler_metadata, torch.int32)
+    _need_cuda("num_splits", num_splits, torch.int32)
+    if q.dim() != 4 or block_table.dim() != 2:
+        raise ValueError("q must be [b, s_q, h_q, d] and block_table [b, max_blocks]")
+    b, s_q, h_q, d = q.shape
+    if kv_pages.dim() != 2 or kv_pages.shape[1] != _lib.MLA_FP8_PAGE_BYTES(d):
+        raise ValueError(f"kv_pages must be [num_blocks, {_lib.MLA_FP8_PAGE_BYTES(d)}] for d = {d}")
+    num_blocks = kv_pages.shape[0]
+    if block_table.shape[0] != b or cache_seqlens.numel() != b or num_splits.numel() != b + 1:
+        raise ValueError("batch size differs between q, block_table, cache_seqlens and num_splits")
+    if tile_scheduler_metadata.dim() != 2 or tile_scheduler_metadata.shape[1] != MLA_METADATA_INTS:
+        raise ValueError("tile_scheduler_metadata must be [num_parts, 8]")
+    num_parts = tile_scheduler_metadata.shape[0]
+    dev = q.device
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((b, s_q, h_q, dv), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((b, s_q, h_q), dtype=torch.float32, device=dev)
+    _need_cuda("out", out, torch.bfloat16)
+    _need_cuda("lse", lse, torch.float32)
+    if tuple(out.shape) != (b, s_q, h_q, dv) or tuple(lse.shape) != (b, s_q, h_q):
+        raise ValueError("out must be [b, s_q, h_q, dv] and lse [b, s_q, h_q]")
+    ws_need = mla_workspace_bytes(b, s_q, h_q, 1, dv, num_parts) if dv == MLA_V_DIM else 256
+    if workspace is None:
+        workspace = torch.empty((ws_need,), dtype=torch.uint8, device=dev)
+    _need_cuda("workspace", workspace, torch.uint8)
+    with torch.cuda.device(dev):
+        st = load().mla_decode_kvcache_fp8(
+            q.data_ptr(), kv_pages.data_ptr(), num_blocks, block_table.data_ptr(), block_table.shape[1],
+            cache_seqlens.data_ptr(), b, s_q, h_q, 1, d, dv, tile_scheduler_metadata.data_ptr(),
+            num_splits.data_ptr(), num_parts, float(softmax_scale), int(bool(causal)), out.data_ptr(),
+            lse.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream_handle(dev))
+    check("mla_decode_kvcache_fp8", st)
+    return out, lse
+
+
 def mla_decode_kvcache_noalloc(q: torch.Tensor, kcache: torch.Tensor, block_table: torch.Tensor,
                                cache_seqlens: torch.Tensor, dv: int, tile_scheduler_metadata: torch.Tensor,
                                num_splits: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,

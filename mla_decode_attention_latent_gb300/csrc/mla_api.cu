@@ -69,7 +69,7 @@ int mla_num_sm_parts(int device, int num_q_rows, int h_kv, int *num_parts) {
     if (device != prev && cudaSetDevice(device) != cudaSuccess) return MLA_ERR_CUDA;
     // one CTA pair (two SMs) per part and row tile: as many pairs as fit at once
     int pairs = 0;
-    cudaError_t e = split_kv_tc_max_pairs<576>(&pairs);  // both row widths fit one CTA per SM
+    cudaError_t e = split_kv_tc_max_pairs<576, false>(&pairs);  // every variant fits one CTA per SM
     if (device != prev) cudaSetDevice(prev);
     if (e != cudaSuccess) return MLA_ERR_CUDA;
     if (pairs < 1) pairs = 1;
@@ -99,11 +99,15 @@ size_t mla_workspace_bytes(int batch, int s_q, int h_q, int h_kv, int dv, int nu
     return workspace_bytes(batch, (int)rows, num_parts);
 }
 
-int mla_decode_kvcache(const void *q, const void *kcache, int64_t num_blocks, const int32_t *block_table,
-                       int max_blocks_per_seq, const int32_t *cache_seqlens, int batch, int s_q, int h_q,
-                       int h_kv, int d, int dv, const int32_t *tile_scheduler_metadata,
-                       const int32_t *num_splits, int num_parts, float softmax_scale, int causal, void *o,
-                       float *lse, void *workspace, size_t ws_bytes, struct CUstream_st *stream) {
+}  // extern "C"
+
+namespace {
+
+// The decode behind both cache formats: validation, then split + combine.
+int decode(const void *q, const void *kcache, bool e4m3, int64_t num_blocks, const int32_t *block_table,
+           int max_blocks_per_seq, const int32_t *cache_seqlens, int batch, int s_q, int h_q, int h_kv, int d, int dv,
+           const int32_t *tile_scheduler_metadata, const int32_t *num_splits, int num_parts, float softmax_scale,
+           int causal, void *o, float *lse, void *workspace, size_t ws_bytes, struct CUstream_st *stream) {
     if (!q || !kcache || !block_table || !cache_seqlens || !tile_scheduler_metadata || !num_splits || !o || !lse ||
         !workspace)
         return MLA_ERR_INVALID_ARG;
@@ -112,6 +116,7 @@ int mla_decode_kvcache(const void *q, const void *kcache, int64_t num_blocks, co
         return MLA_ERR_INVALID_ARG;
     if (!(softmax_scale == softmax_scale)) return MLA_ERR_INVALID_ARG;
     if ((d != kDqk && d != kDv) || dv != kDv || h_kv != 1) return MLA_ERR_UNSUPPORTED;
+    if (e4m3 && d != kDqk) return MLA_ERR_UNSUPPORTED;
     if ((long long)s_q * h_q > kMaxRows) return MLA_ERR_UNSUPPORTED;
     if ((long long)max_blocks_per_seq * kPage > 0x7fffffffLL) return MLA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(kcache) || !aligned16(o) || !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
@@ -148,11 +153,36 @@ int mla_decode_kvcache(const void *q, const void *kcache, int64_t num_blocks, co
         ev_end = g_split_end;
     }
     if (ev_begin && cudaEventRecord(ev_begin, s) != cudaSuccess) return MLA_ERR_CUDA;
-    cudaError_t e = d == kDqk ? launch_split_kv_tc<576>(p, s) : launch_split_kv_tc<512>(p, s);
+    cudaError_t e = e4m3 ? launch_split_kv_tc<576, true>(p, s)
+                         : (d == kDqk ? launch_split_kv_tc<576, false>(p, s) : launch_split_kv_tc<512, false>(p, s));
     if (e != cudaSuccess) return MLA_ERR_CUDA;
     if (ev_end && cudaEventRecord(ev_end, s) != cudaSuccess) return MLA_ERR_CUDA;
     e = launch_combine(p, s);
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_decode_kvcache(const void *q, const void *kcache, int64_t num_blocks, const int32_t *block_table,
+                       int max_blocks_per_seq, const int32_t *cache_seqlens, int batch, int s_q, int h_q,
+                       int h_kv, int d, int dv, const int32_t *tile_scheduler_metadata,
+                       const int32_t *num_splits, int num_parts, float softmax_scale, int causal, void *o,
+                       float *lse, void *workspace, size_t ws_bytes, struct CUstream_st *stream) {
+    return decode(q, kcache, false, num_blocks, block_table, max_blocks_per_seq, cache_seqlens, batch, s_q, h_q, h_kv,
+                  d, dv, tile_scheduler_metadata, num_splits, num_parts, softmax_scale, causal, o, lse, workspace,
+                  ws_bytes, stream);
+}
+
+int mla_decode_kvcache_fp8(const void *q, const void *kv_pages, int64_t num_blocks, const int32_t *block_table,
+                           int max_blocks_per_seq, const int32_t *cache_seqlens, int batch, int s_q, int h_q,
+                           int h_kv, int d, int dv, const int32_t *tile_scheduler_metadata,
+                           const int32_t *num_splits, int num_parts, float softmax_scale, int causal, void *o,
+                           float *lse, void *workspace, size_t ws_bytes, struct CUstream_st *stream) {
+    return decode(q, kv_pages, true, num_blocks, block_table, max_blocks_per_seq, cache_seqlens, batch, s_q, h_q, h_kv,
+                  d, dv, tile_scheduler_metadata, num_splits, num_parts, softmax_scale, causal, o, lse, workspace,
+                  ws_bytes, stream);
 }
 
 int mla_device_status(int *status, int clear) {

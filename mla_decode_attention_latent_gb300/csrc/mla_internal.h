@@ -20,7 +20,7 @@ constexpr int kCombineCost = MLA_SCHED_COMBINE_COST_PAGES;
 // Everything a split-KV kernel needs for one decode call.
 struct DecodeParams {
     const uint16_t *q;            // [batch][s_q][h_q][576] bf16
-    const uint16_t *kcache;       // [num_blocks][64][1][576] bf16
+    const uint16_t *kcache;       // [num_blocks][64][1][576] bf16, or packed e4m3 pages (read as bytes)
     int64_t num_blocks;
     const int32_t *block_table;   // [batch][max_blocks]
     int max_blocks;
@@ -46,12 +46,13 @@ void carve_workspace(void *ws, int batch, int rows, int num_parts, float **o_acc
 
 cudaError_t launch_schedule(const int32_t *seqlens, int batch, int num_parts, int32_t *metadata,
                             int32_t *num_splits, unsigned int *status, cudaStream_t stream);
-// the tensor-core split-KV kernel for cached rows of width D (576 or 512)
-template <int D>
+// the tensor-core split-KV kernel for cached rows of width D (576 or 512), bf16
+// rows or (E4M3, D = 576) packed e4m3 pages with per-token scales
+template <int D, bool E4M3>
 cudaError_t launch_split_kv_tc(const DecodeParams &p, cudaStream_t stream);
 int split_kv_tc_tile_rows();
-// CTA pairs of the split-KV kernel for width D that fit on the current device at once
-template <int D>
+// CTA pairs of the split-KV kernel that fit on the current device at once
+template <int D, bool E4M3>
 cudaError_t split_kv_tc_max_pairs(int *pairs);
 cudaError_t launch_combine(const DecodeParams &p, cudaStream_t stream);
 

@@ -173,6 +173,15 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const vo
         : "memory");
 }
 
+// bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
+// global memory into this CTA's shared memory; completes tx bytes on `bar`
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 // prefetch a contiguous global range into L2
 // bring the line holding `src` into L1 (no register result, never faults)
 __device__ __forceinline__ void prefetch_line_l1(const void *src) {
@@ -196,6 +205,12 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t smem_addr, uint32_t lbo_
 __host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, bool a_mn_major, bool b_mn_major) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
            ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+// instruction descriptor: kind::f16 with f16 A and B (format field 0), fp32 accumulator
+__host__ __device__ constexpr uint32_t idesc_f16(int m, int n, bool a_mn_major, bool b_mn_major) {
+    return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(m >> 4) << 24);
 }
 
 // whole warp: allocate `ncols` TMEM columns; the base address lands in *dst
@@ -350,6 +365,26 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// two bf16 values -> two f16 values (round to nearest even; exact for
+// magnitudes in [2^-17, 65504])
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t x) {
+    return pack_f16(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
+}
+
+// two OCP e4m3 codes (low byte -> low half) -> two f16 values; exact, since
+// every e4m3 value, subnormals included, is an f16 value
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(r) : "r"(pair));
     return r;
 }
 

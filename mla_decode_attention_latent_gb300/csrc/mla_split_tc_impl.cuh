@@ -49,6 +49,16 @@
 //
 // Every wait is bounded (mla_sm103.cuh); on a timeout the kernel raises
 // MLA_DEVERR_TIMEOUT, tells its peer CTA to stop, and unwinds.
+//
+// e4m3 cache (MLA_SPLIT_FP8 = 1, D = 576): a page holds 64 rows of e4m3 codes
+// followed by 64 fp32 per-token scales, and row j dequantizes to c_j * code_j
+// (include/mla_decode.h).  The loads land in the upper half of the same K slots
+// and V stages, and are widened in place to f16 (exact for every e4m3 value):
+// in the score CTA by the whole warp of each TMA producer, in the value CTA by
+// its row warps, which also zero the rows past a sequence's end.  Both MMAs
+// then run in f16 (Q and P rounded to f16).  A token's scale multiplies its
+// score column before the softmax and its P column before P V, so the
+// accumulators see c_j * code_j exactly as the dequantized row.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -71,12 +81,20 @@ using namespace sm103;
 constexpr int kD = MLA_SPLIT_D;                // cached row width: key dims, the first kDv of them the value
 static_assert(kD == 576 || kD == 512, "supported cached row widths");
 constexpr bool kHasRope = kD > kDv;            // a RoPE part beyond the value dims (one more 64-dim chunk)
+#ifndef MLA_SPLIT_FP8
+#define MLA_SPLIT_FP8 0
+#endif
+constexpr bool kFp8 = MLA_SPLIT_FP8 != 0;      // e4m3 cache pages with per-token scales
 
 constexpr int kThreads = 256;                  // 8 warps: TMA, MMA, 4 row warps, second score MMA issuer and TMA producer
 constexpr int kTileRows = 128;                 // query rows per tile = TMEM lanes
-constexpr int kKSlots = 10;                    // score CTA: 16 KB chunk slots, two rings of 5
 constexpr int kScoreIssuers = 2;               // score-CTA MMA issuers (and TMA producers), alternating steps
-constexpr int kRingSlots = 10 / kScoreIssuers;  // slots per score-MMA issuer's ring
+// score CTA: 16 KB MMA operand slots, one ring per issuer: 5 each for a bf16
+// cache; 2 each for an e4m3 cache, whose codes land in separate rings of
+// kLandSlots 8 KB buffers and are widened into these slots
+constexpr int kKSlots = kFp8 ? 4 : 10;
+constexpr int kRingSlots = kKSlots / kScoreIssuers;  // slots per score-MMA issuer's ring
+constexpr int kLandSlots = 6;                        // e4m3: landing buffers per ring
 constexpr int kVStages = 2;                    // value CTA ring: whole pages (dims 0..511)
 constexpr int kSBufs = 2;                      // S buffers in TMEM (score CTA), one per step of two pages
 constexpr int kPBufs = 2;                      // P buffers (staging in the score CTA, landing in the value CTA)
@@ -98,12 +116,25 @@ constexpr float kRescaleLog2 = 8.0f;                       // lazy rescale thres
 constexpr uint32_t kEpiCols = 64;                          // epilogue chunk: 64 fp32 columns
 constexpr uint32_t kEpiStride = kEpiCols * 4 + 16;         // padded row stride (conflict-free v4 stores)
 
+static_assert(!kFp8 || kD == kDqk, "the e4m3 cache holds 576-wide rows");
+constexpr uint32_t kE4PageBytes = kPage * kD + kPage * 4;  // 64 rows of codes, then 64 fp32 scales
+constexpr uint32_t kE4ScaleOff = kPage * kD;               // the scales' byte offset in a page
+constexpr uint32_t kE4ChunkBytes = kPage * 64;             // one 64-dim chunk of one page: 4 KB of codes
+constexpr uint32_t kLandBytes = 2 * kE4ChunkBytes;         // a landing buffer: one chunk of two pages (8 KB)
+constexpr uint32_t kVLandOff = kVStageBytes / 2;           // e4m3 page landing inside a V stage (upper 32 KB)
+constexpr int kScSlots = 8;                                // scale ring: one slot per step of two pages (a producer
+                                                           // waits on the rows of 8 steps back: never in practice)
+constexpr uint32_t kScBytes = 2 * kPage * 4;               // 512 B
+static_assert(kE4PageBytes % 16 == 0 && kE4ScaleOff % 16 == 0, "TMA and bulk-copy alignment of e4m3 pages");
+
 // shared-memory layout (offsets from the 1024-byte aligned base)
 // score CTA: [K rings 2 x 5 x 16 KB][Q RoPE tile 16 KB][P staging 2 x 17 KB]
 constexpr uint32_t kKRingOff = 0;
-constexpr uint32_t kQRopeOff = kKRingOff + kKSlots * kSlotBytes;
+constexpr uint32_t kLandOff = kKRingOff + kKSlots * kSlotBytes;  // e4m3: the landing rings
+constexpr uint32_t kQRopeOff = kLandOff + (kFp8 ? kScoreIssuers * kLandSlots * kLandBytes : 0);
 constexpr uint32_t kStageOff = kQRopeOff + (kHasRope ? kTileRows * 128 : 0);
-constexpr uint32_t kScoreEnd = kStageOff + kPBufs * kPMsgBytes;
+constexpr uint32_t kScaleOff = kStageOff + kPBufs * kPMsgBytes;   // e4m3: per-token scales of the steps in flight
+constexpr uint32_t kScoreEnd = kScaleOff + (kFp8 ? kScSlots * kScBytes : 0);
 // value CTA: [V ring 2 x 64 KB][P landing 2 x 17 KB][epilogue staging 34 KB]
 constexpr uint32_t kVRingOff = 0;
 constexpr uint32_t kPBufOff = kVRingOff + kVStages * kVStageBytes;
@@ -122,8 +153,13 @@ enum Bar {
     B_VFULL = B_PFREE + kPBufs, B_VEMPTY = B_VFULL + kVStages, B_PFULL = B_VEMPTY + kVStages,
     B_PREADY = B_PFULL + kPBufs, B_PVDONE = B_PREADY + kPBufs, B_ODONE = B_PVDONE + 1, B_OEMPTY = B_ODONE + 1,
     // both
-    B_FINAL = B_OEMPTY + 1, B_COUNT = B_FINAL + 1
+    B_FINAL = B_OEMPTY + 1, B_BASE_COUNT = B_FINAL + 1
 };
+// e4m3 cache only: landing of the codes (the converters then arrive on
+// B_KFULL / B_VFULL), and the scale ring of the score CTA
+constexpr int B_KLAND = B_BASE_COUNT, B_VLAND = B_KLAND + kScoreIssuers * kLandSlots, B_SCFULL = B_VLAND + kVStages,
+              B_SCEMPTY = B_SCFULL + kScSlots, B_VREAD = B_SCEMPTY + kScSlots;
+constexpr int B_COUNT = kFp8 ? B_VREAD + 1 : B_BASE_COUNT;
 constexpr uint32_t kTmemSlotOff = kBarOff + B_COUNT * 8;
 constexpr uint32_t kAbortOff = kTmemSlotOff + 4;
 constexpr uint32_t kSmemUsed = kAbortOff + 4;
@@ -218,6 +254,45 @@ __device__ __forceinline__ int safe_block(const DecodeParams &p, int b, int page
     return blk;
 }
 
+// instruction descriptor of both MMAs: bf16 operands, or f16 for the e4m3 cache
+__host__ __device__ constexpr uint32_t idesc_op(int m, int n, bool a_mn_major, bool b_mn_major) {
+    return kFp8 ? idesc_f16(m, n, a_mn_major, b_mn_major) : idesc_bf16(m, n, a_mn_major, b_mn_major);
+}
+
+// In-place widening of e4m3 codes to f16 MMA operand rows.  Row R's 64 codes
+// sit at land + 64 R, as the TMA left them (no swizzle); its 64 f16 values go
+// to base + 128 R with the 128-byte swizzle of the operand descriptors (16-byte
+// piece c of row R at piece c ^ (R % 8)).  The landing area is the upper half
+// of the same buffer, so writing the upper rows overwrites codes: each of the
+// group's kGroup threads reads all of its kItems 16-byte items first (item
+// g = i * kGroup + tid: row g / 4, codes 16 (g % 4) .. + 15), then `sync()`
+// must order every read of the group before any write, then the rows are
+// written.  Rows R with R % 64 >= keep are written as zeros.  Returns false,
+// having written nothing, when `sync()` does.
+template <int kItems, int kGroup, typename Sync>
+__device__ __forceinline__ bool widen_e4m3(uint32_t base, uint32_t land, int tid, int keep, Sync sync) {
+    uint4 x[kItems];
+#pragma unroll
+    for (int i = 0; i < kItems; ++i) x[i] = lds128(land + 16u * (uint32_t)(i * kGroup + tid));
+    if (!sync()) return false;
+#pragma unroll
+    for (int i = 0; i < kItems; ++i) {
+        const int g = i * kGroup + tid;
+        const int R = g >> 2, piece = g & 3;
+        const uint32_t row = base + 128u * (uint32_t)R;
+        uint32_t w[8] = {e4m3x2_to_f16x2(x[i].x), e4m3x2_to_f16x2(x[i].x >> 16), e4m3x2_to_f16x2(x[i].y),
+                         e4m3x2_to_f16x2(x[i].y >> 16), e4m3x2_to_f16x2(x[i].z), e4m3x2_to_f16x2(x[i].z >> 16),
+                         e4m3x2_to_f16x2(x[i].w), e4m3x2_to_f16x2(x[i].w >> 16)};
+        if ((R & (kPage - 1)) >= keep) {
+#pragma unroll
+            for (int t = 0; t < 8; ++t) w[t] = 0u;
+        }
+        sts128(row + 16u * (uint32_t)((2 * piece) ^ (R & 7)), w[0], w[1], w[2], w[3]);
+        sts128(row + 16u * (uint32_t)((2 * piece + 1) ^ (R & 7)), w[4], w[5], w[6], w[7]);
+    }
+    return true;
+}
+
 // -------------------------------------------------------------- roles
 // Score-CTA TMA producers (one lane each, one per MMA issuer's ring `r`,
 // taking the steps of parity r).  A step is up to two consecutive pages
@@ -277,7 +352,116 @@ __device__ void score_producer(const DecodeParams &p, const Ctx &c, const CUtens
         mbar_wait(c.bar(B_KFULL + r * kRingSlots + (int)(k % kRingSlots)), (k / kRingSlots) & 1, c.status);
 }
 
-// Value-CTA TMA producer (one lane): whole pages (dims 0..511) through the V ring.
+// Score-CTA producer for the e4m3 cache; the whole warp runs it.  Lane 0
+// issues each chunk's codes (4 KB per page) into the next buffer of this
+// ring's landing ring, completing on its B_KLAND, and each step's per-token
+// scales (one 256 B bulk copy per page) into the scale ring.  The warp widens
+// the chunks in order, each into the ring's next MMA operand slot once the MMA
+// has freed it (B_KEMPTY), and arrives on the slot's B_KFULL, which the MMA
+// issuer waits for as with a bf16 cache.  A landing buffer is reused as soon as
+// its chunk is widened, so up to kLandSlots chunks are in flight whatever the
+// MMA does.  Block ids come from a window of 32 table entries held one per lane.
+__device__ void score_producer_e4m3(const DecodeParams &p, const Ctx &c, const CUtensorMap *map, int part, int tile,
+                                   int r) {
+    const int lane = threadIdx.x & 31;
+    const uint8_t *kv = reinterpret_cast<const uint8_t *>(p.kcache);
+    PartWalk walk;
+    Segment s;
+    if (lane == 0 && r == 0) {
+        const int rows = min(kTileRows, p.rows - tile * kTileRows);
+        walk.init(p, part);
+        while (walk.next(p, s))
+            if (s.p1 > s.p0 && rows > 0)
+                prefetch_l2(p.q + ((size_t)s.b * p.rows + (size_t)tile * kTileRows) * kD, (uint32_t)rows * kD * 2);
+    }
+    int win_b = -1, win_pg = 0, win_blk = 0;  // lane i holds block_table[win_b][win_pg + i]
+    auto block_of = [&](int b, int pg) -> int {
+        if (b != win_b || pg < win_pg || pg >= win_pg + 32) {
+            win_b = b;
+            win_pg = pg;
+            win_blk = pg + lane < p.max_blocks ? p.block_table[(size_t)b * p.max_blocks + pg + lane] : 0;
+        }
+        int blk = __shfl_sync(0xffffffffu, win_blk, pg - win_pg);
+        if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+            if (lane == 0) atomicOr(p.status, MLA_DEVERR_BLOCK_ID);
+            blk = 0;
+        }
+        return blk;
+    };
+    uint32_t issued = 0, widened = 0;  // chunks of this ring: loaded into the landing ring / widened for the MMA
+    uint32_t two_page = 0;             // bit k % 32: chunk k holds two pages
+    const uint32_t land0 = smem_u32(c.base + kLandOff) + (uint32_t)(r * kLandSlots) * kLandBytes;
+    auto widen_next = [&]() -> bool {
+        const uint32_t k = widened;
+        const int ls = r * kLandSlots + (int)(k % kLandSlots), sl = r * kRingSlots + (int)(k % kRingSlots);
+        if (!warp_wait(c, B_KLAND + ls, (k / kLandSlots) & 1)) return false;
+        if (!warp_wait(c, B_KEMPTY + sl, ((k / kRingSlots) & 1) ^ 1)) return false;
+        const uint32_t slot = smem_u32(c.base + kKRingOff + sl * kSlotBytes);
+        const uint32_t land = land0 + (k % kLandSlots) * kLandBytes;
+        auto sync = [] {
+            __syncwarp();
+            return true;
+        };
+        if ((two_page >> (k & 31)) & 1u) widen_e4m3<16, 32>(slot, land, lane, kPage, sync);
+        else widen_e4m3<8, 32>(slot, land, lane, kPage, sync);
+        // orders this lane's shared-memory writes before the MMA's reads and its
+        // reads of the landing buffer before the next load into it
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(c.bar(B_KFULL + sl));
+        ++widened;
+        return true;
+    };
+    walk.init(p, part);
+    uint32_t step = 0;
+    bool ok = true;
+    while (ok && walk.next(p, s)) {
+        for (int pg = s.p0; ok && pg < s.p1; pg += 2, ++step) {
+            const int npg = min(2, s.p1 - pg);
+            if ((int)(step % kScoreIssuers) != r) continue;  // the other ring's step
+            const int blk0 = block_of(s.b, pg);
+            const int blk1 = npg > 1 ? block_of(s.b, pg + 1) : 0;
+            const int sc = (int)(step % kScSlots);
+            if (!warp_wait(c, B_SCEMPTY + sc, ((step / kScSlots) & 1) ^ 1)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                uint8_t *dst = c.base + kScaleOff + sc * kScBytes;
+                mbar_arrive_expect_tx(c.bar(B_SCFULL + sc), (uint32_t)npg * kPage * 4);
+                bulk_load(dst, kv + (size_t)blk0 * kE4PageBytes + kE4ScaleOff, kPage * 4, c.bar(B_SCFULL + sc));
+                if (npg > 1)
+                    bulk_load(dst + kPage * 4, kv + (size_t)blk1 * kE4PageBytes + kE4ScaleOff, kPage * 4,
+                              c.bar(B_SCFULL + sc));
+            }
+            for (int ch = 0; ch < kKChunks; ++ch) {
+                // the landing buffer of chunk `issued` holds chunk issued - kLandSlots until it is widened
+                while (ok && widened + kLandSlots <= issued) ok = widen_next();
+                if (!ok) break;
+                const uint32_t k = issued;
+                const int ls = r * kLandSlots + (int)(k % kLandSlots);
+                two_page = npg > 1 ? (two_page | (1u << (k & 31))) : (two_page & ~(1u << (k & 31)));
+                if (lane == 0) {
+                    uint8_t *dst = c.base + kLandOff + (size_t)ls * kLandBytes;
+                    mbar_arrive_expect_tx(c.bar(B_KLAND + ls), (uint32_t)npg * kE4ChunkBytes);
+                    tma_load_3d(dst, map, c.bar(B_KLAND + ls), 64 * ch, 0, blk0);
+                    if (npg > 1) tma_load_3d(dst + kE4ChunkBytes, map, c.bar(B_KLAND + ls), 64 * ch, 0, blk1);
+                }
+                ++issued;
+            }
+        }
+    }
+    while (ok && widened < issued) ok = widen_next();
+    // after an early exit, the loads in flight must land before this CTA may exit
+    if (lane == 0)
+        for (uint32_t k = widened; k < issued; ++k)
+            mbar_wait(c.bar(B_KLAND + r * kLandSlots + (int)(k % kLandSlots)), (k / kLandSlots) & 1, c.status);
+    __syncwarp();
+}
+
+// Value-CTA TMA producer (one lane): whole pages (dims 0..511) through the V
+// ring (e4m3 cache: the page's 32 KB of codes into the upper half of the stage,
+// completing on B_VLAND; the row warps widen them and arrive on B_VFULL).
 __device__ void value_producer(const DecodeParams &p, const Ctx &c, const CUtensorMap *map, int part) {
     PartWalk walk;
     Segment s;
@@ -292,14 +476,21 @@ __device__ void value_producer(const DecodeParams &p, const Ctx &c, const CUtens
                 break;
             }
             const int blk = safe_block(p, s.b, pg);
-            mbar_arrive_expect_tx(c.bar(B_VFULL + st), kVStageBytes);
             uint8_t *dst = c.base + kVRingOff + st * kVStageBytes;
-            for (int ch = 0; ch < kVChunks; ++ch)
-                tma_load_3d(dst + ch * kChunkBytes, map, c.bar(B_VFULL + st), 64 * ch, 0, blk);
+            if constexpr (kFp8) {
+                mbar_arrive_expect_tx(c.bar(B_VLAND + st), kVChunks * kE4ChunkBytes);
+                for (int ch = 0; ch < kVChunks; ++ch)
+                    tma_load_3d(dst + kVLandOff + ch * kE4ChunkBytes, map, c.bar(B_VLAND + st), 64 * ch, 0, blk);
+            } else {
+                mbar_arrive_expect_tx(c.bar(B_VFULL + st), kVStageBytes);
+                for (int ch = 0; ch < kVChunks; ++ch)
+                    tma_load_3d(dst + ch * kChunkBytes, map, c.bar(B_VFULL + st), 64 * ch, 0, blk);
+            }
         }
     }
+    constexpr int land = kFp8 ? B_VLAND : B_VFULL;  // the barrier the loads complete on
     for (uint32_t k = it > (uint32_t)kVStages ? it - kVStages : 0; k < it; ++k)
-        mbar_wait(c.bar(B_VFULL + (int)(k % kVStages)), (k / kVStages) & 1, c.status);
+        mbar_wait(c.bar(land + (int)(k % kVStages)), (k / kVStages) & 1, c.status);
 }
 
 // Score-CTA MMA issuers: S[buf] = Q K^T for every step of (up to) two pages:
@@ -335,8 +526,8 @@ __device__ void score_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, in
             const int sb = (int)(st % kSBufs);
             const uint32_t d = tmem + kSCol0 + sb * kSCols;
             const int npg = min(2, s.p1 - (s.p0 + 2 * j));
-            const uint32_t idesc = npg == 2 ? idesc_bf16(kTileRows, 2 * kPage, false, false)
-                                            : idesc_bf16(kTileRows, kPage, false, false);
+            const uint32_t idesc = npg == 2 ? idesc_op(kTileRows, 2 * kPage, false, false)
+                                            : idesc_op(kTileRows, kPage, false, false);
             if (!wait(c, B_SEMPTY + sb, ((st / kSBufs) & 1) ^ 1)) return;
             tc_fence_after();  // the row warps' reads of this S buffer come first
             for (int ch = 0; ch < kKChunks; ++ch, ++ring_it) {
@@ -370,7 +561,7 @@ __device__ void score_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, in
 // without pages never waits on this thread, and counting it would let the row
 // warps complete two phases of the O-free barrier between two of its waits.
 __device__ void value_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, int part) {
-    constexpr uint32_t idesc = idesc_bf16(kTileRows, 256, false, true);
+    constexpr uint32_t idesc = idesc_op(kTileRows, 256, false, true);
     PartWalk walk;
     walk.init(p, part);
     Segment s;
@@ -426,8 +617,9 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
         ++seg;
         if (s.p1 > s.p0) {
             // Q row r: latent dims 0..511 into TMEM lane r (columns 0..255,
-            // bf16 pairs), RoPE dims 512..575 into row r of the swizzled smem
-            // tile; four 64-dim chunks (32 loads) in flight at a time
+            // bf16 pairs, or f16 pairs for the e4m3 cache), RoPE dims 512..575
+            // into row r of the swizzled smem tile; four 64-dim chunks (32
+            // loads) in flight at a time
             const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q + ((size_t)s.b * p.rows + (row_ok ? gr : 0)) * kD);
 #pragma unroll 1
             for (int ch0 = 0; ch0 < kLatChunks; ch0 += 4) {
@@ -444,14 +636,23 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
                         v[4 * j + 2] = x[8 * k + j].z;
                         v[4 * j + 3] = x[8 * k + j].w;
                     }
+                    if constexpr (kFp8) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = bf16x2_to_f16x2(v[j]);
+                    }
                     tmem_st32(tmem + lane_base + (ch0 + k) * 32, v);
                 }
             }
             if constexpr (kHasRope) {
                 uint4 *rope = reinterpret_cast<uint4 *>(c.base + kQRopeOff + r * 128);
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    rope[j ^ (r & 7)] = row_ok ? __ldg(qrow + kLatChunks * 8 + j) : make_uint4(0, 0, 0, 0);
+                for (int j = 0; j < 8; ++j) {
+                    uint4 y = row_ok ? __ldg(qrow + kLatChunks * 8 + j) : make_uint4(0, 0, 0, 0);
+                    if constexpr (kFp8)
+                        y = make_uint4(bf16x2_to_f16x2(y.x), bf16x2_to_f16x2(y.y), bf16x2_to_f16x2(y.z),
+                                       bf16x2_to_f16x2(y.w));
+                    rope[j ^ (r & 7)] = y;
+                }
                 fence_proxy_async_smem();
             }
             tmem_wait_st();
@@ -464,7 +665,9 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
             const int pb = it % kPBufs;
             const int q2 = (pg - s.p0) & 1;          // position of this page in its step
             const int sb = step % kSBufs;
+            const int scs = (int)(step % kScSlots);  // e4m3: this step's slot in the scale ring
             if (q2 == 0 && !warp_wait(c, B_SFULL + sb, (step / kSBufs) & 1)) return;
+            if (kFp8 && q2 == 0 && !warp_wait(c, B_SCFULL + scs, (step / kScSlots) & 1)) return;
             tc_fence_after();
             uint32_t sr[64];
             {
@@ -473,16 +676,47 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
                 tmem_ld32(tmem + lane_base + kSCol0 + sb * kSCols + q2 * kPage, lo);
                 tmem_ld32(tmem + lane_base + kSCol0 + sb * kSCols + q2 * kPage + 32, hi);
             }
+            // keys of this page visible to this row
+            int nvalid = row_ok ? T_row - pg * kPage : 0;
+            nvalid = nvalid < 0 ? 0 : (nvalid > kPage ? kPage : nvalid);
+            // e4m3 cache: the page's per-token scales (those of keys past the
+            // visible ones, whatever the page holds there, read as 0)
+            float cs[kFp8 ? kPage : 1];
+            if constexpr (kFp8) {
+                const uint32_t sc_s = smem_u32(c.base + kScaleOff) + (uint32_t)scs * kScBytes + (uint32_t)q2 * kPage * 4;
+#pragma unroll
+                for (int j = 0; j < kPage / 4; ++j) {
+                    const uint4 c4 = lds128(sc_s + 16 * j);
+                    cs[4 * j] = __uint_as_float(c4.x);
+                    cs[4 * j + 1] = __uint_as_float(c4.y);
+                    cs[4 * j + 2] = __uint_as_float(c4.z);
+                    cs[4 * j + 3] = __uint_as_float(c4.w);
+                }
+                if (nvalid < kPage) {
+#pragma unroll
+                    for (int j = 0; j < kPage; ++j) cs[j] = j < nvalid ? cs[j] : 0.f;
+                }
+            }
             tmem_wait_ld();
             if (q2 == 1 || pg == s.p1 - 1) {         // last page of the step: release its S buffer
                 tc_fence_before();
                 mbar_arrive(c.bar(B_SEMPTY + sb));
+                if constexpr (kFp8) mbar_arrive(c.bar(B_SCEMPTY + scs));  // the scales are in registers
                 ++step;
             }
-
-            // keys of this page visible to this row
-            int nvalid = row_ok ? T_row - pg * kPage : 0;
-            nvalid = nvalid < 0 ? 0 : (nvalid > kPage ? kPage : nvalid);
+            if constexpr (kFp8) {
+                // score of key j times its token's scale: the dequantized key
+                const uint64_t zero2 = f2_pack(0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    float xa, xb;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1])),
+                                     f2_pack(cs[2 * j], cs[2 * j + 1]), zero2),
+                              xa, xb);
+                    sr[2 * j] = __float_as_uint(xa);
+                    sr[2 * j + 1] = __float_as_uint(xb);
+                }
+            }
             const float sc = p.scale_log2;
             // page maximum of scale * log2(e) * s over the visible keys, four
             // independent chains to keep the dependency depth short.  A full
@@ -521,7 +755,15 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
                     f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * j]), __uint_as_float(sr[2 * j + 1])), sc2, nm2), xa, xb);
                     const float a = ex2(xa), b = ex2(xb);
                     sum2[j & 3] = f2_add(sum2[j & 3], f2_pack(a, b));
-                    pk[j] = pack_bf16(a, b);
+                    if constexpr (kFp8) {
+                        // P of key j times its token's scale: the dequantized value row
+                        float pa, pb2;
+                        f2_unpack(f2_fma(f2_pack(a, b), f2_pack(cs[2 * j], cs[2 * j + 1]), f2_pack(0.f, 0.f)), pa,
+                                  pb2);
+                        pk[j] = pack_f16(pa, pb2);
+                    } else {
+                        pk[j] = pack_bf16(a, b);
+                    }
                 }
             }
             float sum_lo, sum_hi;
@@ -572,7 +814,8 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
         if (!warp_wait<true>(c, B_PFREE + (int)(k % kPBufs), (k / kPBufs) & 1)) return;
 }
 
-// Value-CTA row warps: V tail zeroing, lazy O rescale, epilogue.
+// Value-CTA row warps: V tail zeroing (e4m3 cache: widening of each V page),
+// lazy O rescale, epilogue.
 __device__ void value_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, int part, int tile) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = 32 * (warp & 3) + lane;
@@ -587,6 +830,20 @@ __device__ void value_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
         float inv_l = 0.f;
         for (int pg = s.p0; pg < s.p1; ++pg, ++it) {
             const int pb = it % kPBufs, st = it % kVStages;
+            if constexpr (kFp8) {
+                // widen the page's V codes in place as soon as they land (rows
+                // past the sequence's end become zeros); the 128 threads' reads
+                // all come before any write through B_VREAD, a bounded barrier
+                if (!warp_wait(c, B_VLAND + st, (it / kVStages) & 1)) return;
+                const uint32_t stage = smem_u32(c.base + kVRingOff + st * kVStageBytes);
+                const bool ok = widen_e4m3<16, 128>(stage, stage + kVLandOff, tid, min(s.T - pg * kPage, kPage), [&] {
+                    mbar_arrive(c.bar(B_VREAD));
+                    return warp_wait(c, B_VREAD, it & 1);
+                });
+                if (!ok) return;
+                fence_proxy_async_smem();
+                mbar_arrive(c.bar(B_VFULL + st));
+            }
             if (!warp_wait<true>(c, B_PFULL + pb, (it / kPBufs) & 1)) return;
             const uint32_t buf_s = smem_u32(c.base + kPBufOff + pb * kPMsgBytes);
             const float fac = __uint_as_float(lds32(buf_s + kFacOff + 4 * r));
@@ -594,7 +851,7 @@ __device__ void value_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
             // rows past the sequence's end in its last page: zero them in V so
             // that garbage (even NaN) times a zero weight stays zero
             const int tail = s.T - pg * kPage;
-            if (tail < kPage) {
+            if (!kFp8 && tail < kPage) {
                 if (!warp_wait(c, B_VFULL + st, (it / kVStages) & 1)) return;
                 uint8_t *vt = c.base + kVRingOff + st * kVStageBytes;
                 const int rows_bad = kPage - tail;
@@ -745,8 +1002,17 @@ split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParam
             mbar_init(c.bar(B_KEMPTY + i), 1);
         }
         for (int i = 0; i < kVStages; ++i) {
-            mbar_init(c.bar(B_VFULL + i), 1);
+            mbar_init(c.bar(B_VFULL + i), kFp8 ? 128 : 1);  // e4m3: the 128 row threads that widened the page
             mbar_init(c.bar(B_VEMPTY + i), 1);
+        }
+        if constexpr (kFp8) {
+            for (int i = 0; i < kScoreIssuers * kLandSlots; ++i) mbar_init(c.bar(B_KLAND + i), 1);
+            for (int i = 0; i < kVStages; ++i) mbar_init(c.bar(B_VLAND + i), 1);
+            for (int i = 0; i < kScSlots; ++i) {
+                mbar_init(c.bar(B_SCFULL + i), 1);
+                mbar_init(c.bar(B_SCEMPTY + i), 128);
+            }
+            mbar_init(c.bar(B_VREAD), 128);
         }
         for (int i = 0; i < kSBufs; ++i) {
             mbar_init(c.bar(B_SFULL + i), 1);
@@ -786,7 +1052,9 @@ split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParam
     griddep_wait();
 
     if (warp == 0 || warp == 7) {
-        if (elect_one_lane() && (warp == 0 || (is_score && kScoreIssuers > 1))) {
+        if (kFp8 && is_score) {
+            score_producer_e4m3(p, c, &kv_map, part, tile, warp == 0 ? 0 : 1);
+        } else if (elect_one_lane() && (warp == 0 || (is_score && kScoreIssuers > 1))) {
             if (is_score) score_producer(p, c, &kv_map, part, tile, warp == 0 ? 0 : 1);
             else value_producer(p, c, &kv_map, part);
         }
@@ -833,9 +1101,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // kcache [num_blocks][64][D] bf16 viewed as a 3-D tensor {D, 64, num_blocks};
 // one box is a 64-dim x 64-token chunk, stored with the 128-byte swizzle that
 // the tcgen05 K-major (K) and MN-major (V) operand descriptors expect.
+// e4m3 pages: the codes of a page viewed as {D bytes, 64, num_blocks} with the
+// page stride; a box (64 codes x 64 tokens) lands unswizzled, 64 B per token.
 bool make_kv_map(CUtensorMap *m, const void *kcache, int64_t num_blocks) {
     auto enc = encode_fn();
     if (!enc) return false;
+    if constexpr (kFp8) {
+        cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)kPage, (cuuint64_t)num_blocks};
+        cuuint64_t strides[2] = {(cuuint64_t)kD, (cuuint64_t)kE4PageBytes};
+        cuuint32_t box[3] = {64, (cuuint32_t)kPage, 1};
+        cuuint32_t es[3] = {1, 1, 1};
+        return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(kcache), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
     cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)kPage, (cuuint64_t)num_blocks};
     cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)kPage * kD * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)kPage, 1};
@@ -861,7 +1140,7 @@ cudaError_t prepare(int dev) {
 }  // namespace
 
 template <>
-cudaError_t split_kv_tc_max_pairs<kD>(int *pairs) {
+cudaError_t split_kv_tc_max_pairs<kD, kFp8>(int *pairs) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -891,7 +1170,7 @@ cudaError_t split_kv_tc_max_pairs<kD>(int *pairs) {
 }
 
 template <>
-cudaError_t launch_split_kv_tc<kD>(const DecodeParams &p, cudaStream_t stream) {
+cudaError_t launch_split_kv_tc<kD, kFp8>(const DecodeParams &p, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

@@ -53,10 +53,15 @@ def assert_parity(o, lse, o_ref, lse_ref, what=""):
     assert not errs, f"{what}: " + "; ".join(errs)
 
 
+def _oracle_call(c: W.Case, q, kcache, bt, sl, rows=None):
+    if c.fp8:
+        return oracle.mla_decode_fp8(W.bf16_bits(q), kcache.cpu().numpy(), bt, sl, c.dv, c.softmax_scale, c.causal,
+                                     rows=rows)
+    return oracle.mla_decode(W.bf16_bits(q), W.bf16_bits(kcache), bt, sl, c.dv, c.softmax_scale, c.causal, rows=rows)
+
+
 def oracle_of(x: W.Inputs, rows=None):
-    c = x.case
-    return oracle.mla_decode(W.bf16_bits(x.q), W.bf16_bits(x.kcache), x.block_table.cpu().numpy(),
-                             x.cache_seqlens.cpu().numpy(), c.dv, c.softmax_scale, c.causal, rows=rows)
+    return _oracle_call(x.case, x.q, x.kcache, x.block_table.cpu().numpy(), x.cache_seqlens.cpu().numpy(), rows)
 
 
 def to_device(x: W.Inputs, dev) -> W.Inputs:
@@ -67,8 +72,9 @@ def run_gpu(x: W.Inputs, num_parts=None):
     import mla_decode_attention_latent_gb300 as mla
     c = x.case
     md, ns = mla.mla_get_metadata(x.cache_seqlens, c.num_q_rows, c.h_kv, num_parts=num_parts)
-    o, lse = mla.mla_decode_kvcache(x.q, x.kcache, x.block_table, x.cache_seqlens, c.dv, md, ns,
-                                    softmax_scale=c.softmax_scale, causal=c.causal)
+    decode = mla.mla_decode_kvcache_fp8 if c.fp8 else mla.mla_decode_kvcache
+    o, lse = decode(x.q, x.kcache, x.block_table, x.cache_seqlens, c.dv, md, ns, softmax_scale=c.softmax_scale,
+                    causal=c.causal)
     torch.cuda.synchronize()
     st = mla.mla_device_status(clear=True)
     return o, lse, md, ns, st
@@ -105,6 +111,6 @@ def sampled_oracle(x: W.Inputs, seqs, rows_per_seq, rng):
         for r in sorted(pick):
             local_rows.append(i * R + r)
             full_rows.append(b * R + r)
-    o_ref, lse_ref = oracle.mla_decode(W.bf16_bits(q), W.bf16_bits(kc), bt_c, sl[list(seqs)].astype(np.int32),
-                                       c.dv, c.softmax_scale, c.causal, rows=np.array(local_rows, np.int64))
+    o_ref, lse_ref = _oracle_call(c, q, kc, bt_c, sl[list(seqs)].astype(np.int32),
+                                  rows=np.array(local_rows, np.int64))
     return np.array(full_rows, np.int64), o_ref, lse_ref

@@ -115,3 +115,30 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros(4, dtype=torch.int32)
     with pytest.raises(ValueError, match="CUDA tensor"):
         mla.mla_get_metadata(x, 16, 1, num_parts=3)
+
+
+def _decode_fp8(lib, **over):
+    a = dict(q=16, kv=16, num_blocks=4, bt=16, max_blocks=2, sl=16, batch=2, s_q=1, h_q=16, h_kv=1, d=576,
+             dv=512, md=16, ns=16, num_parts=3, scale=1 / 24, causal=0, o=16, lse=16, ws=256, ws_bytes=1 << 30)
+    a.update(over)
+    return lib.mla_decode_kvcache_fp8(a["q"], a["kv"], a["num_blocks"], a["bt"], a["max_blocks"], a["sl"], a["batch"],
+                                      a["s_q"], a["h_q"], a["h_kv"], a["d"], a["dv"], a["md"], a["ns"],
+                                      a["num_parts"], a["scale"], a["causal"], a["o"], a["lse"], a["ws"],
+                                      a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(kv=None), _lib.MLA_ERR_INVALID_ARG),
+    (dict(kv=24), _lib.MLA_ERR_INVALID_ARG),           # packed pages must be 16-byte aligned
+    (dict(d=512), _lib.MLA_ERR_UNSUPPORTED),           # e4m3 pages hold 576-wide rows only
+    (dict(dv=256), _lib.MLA_ERR_UNSUPPORTED),
+    (dict(ws_bytes=1024), _lib.MLA_ERR_WORKSPACE),
+])
+def test_fp8_decode_rejects_bad_arguments_before_launch(lib, over, code):
+    assert _decode_fp8(lib, **over) == code
+
+
+def test_fp8_page_bytes():
+    text = open(HEADER).read()
+    assert "#define MLA_FP8_PAGE_BYTES(d) (MLA_PAGE_SIZE * (d) + MLA_PAGE_SIZE * 4)" in text
+    assert _lib.MLA_FP8_PAGE_BYTES(576) == 37120

@@ -227,7 +227,7 @@ def test_empty_segments_between_full_ones():
             assert torch.equal(o, o2) and torch.equal(lse, l2), parts
 
 
-@pytest.mark.parametrize("name", ["uniform", "variable", "mtp", "long", "uniform_d512"])
+@pytest.mark.parametrize("name", ["uniform", "variable", "mtp", "long", "uniform_d512", "uniform_fp8"])
 def test_full_size_repeatable(name):
     # bit-identical outputs over repeated launches at full size: every wait
     # on the hand-offs between the two CTAs of a pair has to be exact
@@ -244,7 +244,7 @@ def test_full_size_repeatable(name):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("name", ["uniform", "variable", "mtp", "long", "uniform_d512"])
+@pytest.mark.parametrize("name", ["uniform", "variable", "mtp", "long", "uniform_d512", "uniform_fp8"])
 def test_full_size_sampled(name):
     c = W.CASES[name]
     x = W.make_inputs(c, device="cuda")
@@ -260,3 +260,58 @@ def test_full_size_sampled(name):
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
     del x, o, lse
     torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------- e4m3 cache
+def fp8_case(name, batch, s_q, h_q, seqlens, causal=False, seed=120, pool_pages=None):
+    return dataclasses.replace(case(name, batch, s_q, h_q, seqlens, causal=causal, seed=seed, pool_pages=pool_pages),
+                               fp8=True)
+
+
+@pytest.mark.parametrize("batch,s_q,h_q,seqlens,causal,parts", [
+    (2, 1, 16, [100, 37], False, None),           # the tiny shape
+    (3, 1, 128, [1000, 77, 2100], False, 1),      # one part walks every sequence
+    (3, 1, 128, [1000, 77, 2100], False, 3),      # sequences cut between parts
+    (3, 1, 128, [1000, 77, 2100], False, None),
+    (2, 4, 32, [513, 70], True, None),            # multi-token, causal
+    (2, 3, 20, [300, 65], True, 2),               # a partial row tile
+    (4, 1, 32, [0, 1, 63, 65], False, None),      # empty, one-key and ragged pages
+    (2, 2, 128, [129, 64], True, None),           # two row tiles
+])
+def test_fp8_cache(batch, s_q, h_q, seqlens, causal, parts):
+    check(fp8_case("fp8", batch, s_q, h_q, seqlens, causal=causal, seed=121 + batch + s_q), num_parts=parts)
+
+
+def test_fp8_garbage_past_the_end():
+    # NaN codes and NaN scales in the rows past each sequence's end and in
+    # every unused page must not reach the output
+    page_bytes, scale_off = _lib.MLA_FP8_PAGE_BYTES(576), 64 * 576
+
+    def poison(x):
+        sl = x.cache_seqlens.tolist()
+        bt = x.block_table
+        used = set()
+        for b, t in enumerate(sl):
+            n = (t + 63) // 64
+            used.update(bt[b, :n].tolist())
+            if t % 64:
+                blk = int(bt[b, n - 1])
+                x.kcache[blk, (t % 64) * 576:scale_off] = 0x7F
+                x.kcache[blk, scale_off + 4 * (t % 64):page_bytes] = 0xFF
+        for p in range(x.kcache.shape[0]):
+            if p not in used:
+                x.kcache[p] = 0xFF
+    c = fp8_case("fp8-nan-tail", 3, 2, 64, [100, 37, 250], causal=True, seed=130, pool_pages=12)
+    check(c, mutate=poison)
+
+
+def test_fp8_deterministic_and_split_invariant():
+    c = fp8_case("fp8-det", 2, 1, 128, [3000, 1500], seed=131)
+    x = to_device(W.make_inputs(c, "cpu"), DEV)
+    o1, l1, *_ = run_gpu(x, num_parts=1)
+    o1b, l1b, *_ = run_gpu(x, num_parts=1)
+    assert torch.equal(o1, o1b) and torch.equal(l1, l1b)
+    for p in (2, 40):
+        o2, l2, *_ = run_gpu(x, num_parts=p)
+        assert torch.allclose(o1.float(), o2.float(), rtol=1e-2, atol=2e-3)
+        assert torch.allclose(l1, l2, atol=1e-4)
