@@ -49,6 +49,17 @@ def test_roofline_bound_follows_arithmetic_intensity():
     assert achieved == pytest.approx(mtp["flops"] / 5e-4 / 1e12)
 
 
+def test_fp8_figures_count_packed_pages():
+    # e4m3 pages: 64 x 576 codes + 64 fp32 scales = 37,120 B; FLOPs as for bf16,
+    # so the halved bytes put the workload above the ridge (tensor roof)
+    fig = bench.workload_figures(W.UNIFORM_FP8, seqlens_of(W.UNIFORM_FP8))
+    assert fig["kv_bytes"] == 64 * 64 * 37120
+    assert fig["bytes"] == 64 * 64 * 37120 + 64 * 128 * (576 * 2 + 512 * 2 + 4)
+    assert fig["flops"] == bench.workload_figures(W.UNIFORM, seqlens_of(W.UNIFORM))["flops"]
+    assert bench.roofline(fig, 0.2, FALLBACK)[0] == "tensor"
+    assert "e4m3" in bench.workload_label(W.UNIFORM_FP8)
+
+
 def test_workload_label_names_the_sizes():
     label = bench.workload_label(W.UNIFORM_D512)
     assert label.startswith("uniform_d512: b=64, s_q=1, h_q=128") and "d=512" in label
