@@ -11,6 +11,8 @@ Contents
   ``mla_decode``   the decode definition in fp64 (plain C, ``mla_oracle.c``)
   ``mla_decode_fp8``  the same over packed e4m3 pages with per-token scales
   ``e4m3_to_float64``  the OCP e4m3 decoding the fp8 path uses
+  ``mla_decode_sparse``  sparse top-k decode: each query token attends to the
+                   token positions its index list names
   ``schedule``     the split-KV work partition restated in plain Python
                    (``schedule.py``)
 
@@ -63,6 +65,14 @@ def load_library(path: str):
     ]
     lib.oracle_mla_decode_fp8.restype = ctypes.c_int
     lib.oracle_mla_decode_fp8.argtypes = lib.oracle_mla_decode.argtypes
+    lib.oracle_mla_decode_sparse.restype = ctypes.c_int
+    lib.oracle_mla_decode_sparse.argtypes = [
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+        ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_double, ctypes.c_void_p, ctypes.c_int64,
+        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+    ]
     lib.oracle_e4m3_to_double.restype = ctypes.c_double
     lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
     lib.oracle_max_threads.restype = ctypes.c_int
@@ -139,6 +149,36 @@ def mla_decode_fp8(q_bits, kv_pages, block_table, cache_seqlens, dv, softmax_sca
         o.ctypes.data, lse.ctypes.data, int(nthreads))
     if st != 0:
         raise ValueError(f"oracle_mla_decode_fp8 failed with status {st}")
+    return o, lse
+
+
+def mla_decode_sparse(q_bits, kcache_bits, block_table, cache_seqlens, indices, dv, softmax_scale,
+                      rows=None, nthreads=0, lib=None):
+    """fp64 sparse top-k MLA decode (see ``mla_oracle.c``).
+
+    indices  int32 [b, s_q, topk]: token positions each query token attends to
+             (entries outside [0, cache_seqlens[b]) are ignored)
+    Other arguments and the result as ``mla_decode`` (no causal flag).
+    """
+    q = _bits(q_bits)
+    k = _bits(kcache_bits)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(cache_seqlens, dtype=np.int32)
+    idx = np.ascontiguousarray(indices, dtype=np.int32)
+    b, s_q, h_q, d = q.shape
+    num_blocks, page, h_kv, dk = k.shape
+    if dk != d:
+        raise ValueError("q and kcache disagree on the head dimension")
+    if idx.ndim != 3 or idx.shape[:2] != (b, s_q):
+        raise ValueError("indices must be [b, s_q, topk]")
+    o, lse, rows_arr, n_rows = _outputs(q, bt, sl, dv, rows)
+    st = (lib or _load()).oracle_mla_decode_sparse(
+        q.ctypes.data, k.ctypes.data, num_blocks, page, bt.ctypes.data, bt.shape[1],
+        sl.ctypes.data, idx.ctypes.data, idx.shape[2], b, s_q, h_q, h_kv, d, dv, float(softmax_scale),
+        None if rows_arr is None else rows_arr.ctypes.data, n_rows,
+        o.ctypes.data, lse.ctypes.data, int(nthreads))
+    if st != 0:
+        raise ValueError(f"oracle_mla_decode_sparse failed with status {st}")
     return o, lse
 
 

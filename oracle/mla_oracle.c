@@ -46,6 +46,20 @@
  * unchanged.  e4m3 is the OCP 8-bit float E4M3: sign bit, 4 exponent bits with
  * bias 7, 3 mantissa bits; exponent 0 encodes subnormals m/8 * 2^-6; S.1111.111
  * is NaN; there are no infinities (largest finite value 448).
+ *
+ * Sparse top-k decode (oracle_mla_decode_sparse).  "[flashinfer] FlashInfer,
+ * SM120 GPU를 위한 희소 MLA 커널 추가로 LLM 추론 속도 향상" (section "왜 이게
+ * 좋은가?", item 2) describes sparse MLA as attention over only some tokens of
+ * the KV cache, chosen by top-k selection, for paged caches with d_qk = 576
+ * and 512; it gives no interface.  The reading taken: query token i of
+ * sequence b carries a list indices[b][i][0 .. topk) of token positions in
+ * the sequence, shared by all of its heads; entries outside [0, T_b) (T_b =
+ * cache_seqlens[b]; -1 pads short lists) are ignored, every other entry is one
+ * term of the softmax (a position listed twice counts twice), and no causal
+ * mask applies on top of the list:
+ *     s_t = scale * <q, k_{indices[t]}>,  LSE = ln sum_t exp(s_t),
+ *     O = sum_t exp(s_t - LSE) * v_{indices[t]}       over the valid entries t.
+ * A row with no valid entry has O = 0 and LSE = -inf.
  */
 #include <math.h>
 #include <stdint.h>
@@ -238,6 +252,115 @@ int oracle_mla_decode_fp8(const uint16_t *q, const uint8_t *kv_pages, int64_t nu
     cache_view cv = {NULL, kv_pages};
     return decode_rows(q, &cv, num_blocks, page, block_table, max_blocks, cache_seqlens, batch, s_q, h_q,
                        h_kv, d, dv, scale, causal, rows, n_rows, o, lse, nthreads);
+}
+
+/* One output row of the sparse decode (definition in the header comment). */
+static int oracle_one_row_sparse(const uint16_t *q, const cache_view *cv, int64_t num_blocks, int page,
+                                 const int32_t *block_table, int max_blocks, const int32_t *cache_seqlens,
+                                 const int32_t *indices, int topk, int s_q, int h_q, int h_kv, int d, int dv,
+                                 double scale, int64_t r, double *o_row, double *lse_row, double *scores,
+                                 int64_t *keys, double *krow) {
+    int64_t h = r % h_q;
+    int64_t i = (r / h_q) % s_q;
+    int64_t b = r / ((int64_t)h_q * s_q);
+    int64_t g = h / (h_q / h_kv);
+    int64_t T = cache_seqlens[b];
+    const int32_t *list = indices + (b * s_q + i) * (int64_t)topk;
+    const uint16_t *qrow = q + r * (int64_t)d;
+
+    for (int v = 0; v < dv; ++v) o_row[v] = 0.0;
+    /* the valid entries, in list order */
+    int n = 0;
+    for (int t = 0; t < topk; ++t)
+        if (list[t] >= 0 && list[t] < T) keys[n++] = list[t];
+    if (n == 0) {
+        *lse_row = -INFINITY;
+        return ORACLE_OK;
+    }
+    for (int t = 0; t < n; ++t) {
+        int64_t j = keys[t];
+        int64_t blk = block_table[b * max_blocks + j / page];
+        if (blk < 0 || blk >= num_blocks) return ORACLE_ERR_BLOCK;
+        load_row(cv, blk, page, j % page, h_kv, g, d, krow);
+        double acc = 0.0;
+        for (int c = 0; c < d; ++c) acc += bf16_bits_to_double(qrow[c]) * krow[c];
+        scores[t] = scale * acc;
+    }
+    double M = scores[0];
+    for (int t = 1; t < n; ++t)
+        if (scores[t] > M) M = scores[t];
+    double sum = 0.0;
+    for (int t = 0; t < n; ++t) sum += exp(scores[t] - M);
+    double lse = M + log(sum);
+    *lse_row = lse;
+    for (int t = 0; t < n; ++t) {
+        int64_t j = keys[t];
+        int64_t blk = block_table[b * max_blocks + j / page];
+        load_row(cv, blk, page, j % page, h_kv, g, d, krow);
+        double w = exp(scores[t] - lse);
+        for (int v = 0; v < dv; ++v) o_row[v] += w * krow[v];
+    }
+    return ORACLE_OK;
+}
+
+/*
+ * Sparse top-k decode over a bf16 cache: as oracle_mla_decode, plus
+ *   indices  [batch, s_q, topk] int32 token positions per query token
+ * (no causal flag: the lists decide what each query token sees).
+ */
+int oracle_mla_decode_sparse(const uint16_t *q, const uint16_t *kcache, int64_t num_blocks, int page,
+                             const int32_t *block_table, int max_blocks, const int32_t *cache_seqlens,
+                             const int32_t *indices, int topk, int batch, int s_q, int h_q, int h_kv, int d,
+                             int dv, double scale, const int64_t *rows, int64_t n_rows, double *o, double *lse,
+                             int nthreads) {
+    if (!q || !kcache || !block_table || !cache_seqlens || !indices || !o || !lse) return ORACLE_ERR_ARG;
+    if (batch < 0 || s_q <= 0 || h_q <= 0 || h_kv <= 0 || h_q % h_kv || d <= 0 || dv <= 0 || dv > d ||
+        page <= 0 || max_blocks < 0 || topk < 0)
+        return ORACLE_ERR_ARG;
+    int64_t total_rows = (int64_t)batch * s_q * h_q;
+    if (!rows) n_rows = total_rows;
+    for (int b = 0; b < batch; ++b)
+        if (cache_seqlens[b] < 0 || (int64_t)cache_seqlens[b] > (int64_t)max_blocks * page) return ORACLE_ERR_ARG;
+    for (int64_t n = 0; rows && n < n_rows; ++n)
+        if (rows[n] < 0 || rows[n] >= total_rows) return ORACLE_ERR_ARG;
+    cache_view cv = {kcache, NULL};
+    int status = ORACLE_OK;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads)
+#endif
+    {
+        size_t nk = (size_t)(topk > 0 ? topk : 1);
+        double *scores = (double *)malloc(sizeof(double) * nk);
+        int64_t *keys = (int64_t *)malloc(sizeof(int64_t) * nk);
+        double *krow = (double *)malloc(sizeof(double) * (size_t)d);
+        if (!scores || !keys || !krow) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            status = ORACLE_ERR_NOMEM;
+        }
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t n = 0; n < n_rows; ++n) {
+            if (!scores || !keys || !krow) continue;
+            int64_t r = rows ? rows[n] : n;
+            int st = oracle_one_row_sparse(q, &cv, num_blocks, page, block_table, max_blocks, cache_seqlens,
+                                           indices, topk, s_q, h_q, h_kv, d, dv, scale, r, o + n * (int64_t)dv,
+                                           lse + n, scores, keys, krow);
+            if (st != ORACLE_OK) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+                status = st;
+            }
+        }
+        free(scores);
+        free(keys);
+        free(krow);
+    }
+    return status;
 }
 
 /* Threads the oracle will use by default (for reporting the CPU baseline). */

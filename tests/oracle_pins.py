@@ -32,6 +32,16 @@ e4m3 decode and the oracle's e4m3 code decoder):
   pin_fp8_scale_linearity  doubling every token's scale and halving q leaves
                          the scores unchanged and doubles O exactly
 
+Pins of the sparse top-k decode (``SPARSE_PINS``; they take the dense and the
+sparse decode):
+
+  pin_sparse_brute_force   numpy gather-and-softmax over each query token's
+                           list (entries outside [0, T) dropped, repeats kept)
+  pin_sparse_full_list     the list 0 .. T-1 (padded with -1) gives the dense
+                           decode bit for bit
+  pin_sparse_order         permuting a list changes nothing beyond rounding;
+                           appending ignored entries changes no bit
+
 The mutation test in ``test_oracle_pins.py`` plants mistakes in a copy of the
 oracle's C source and checks that some pin catches each one.
 """
@@ -411,3 +421,102 @@ def pin_fp8_scale_linearity(decode, decode_fp8, e4m3, seed=22):
 
 
 FP8_PINS = [pin_e4m3_codes, pin_fp8_matches_bf16, pin_fp8_scale_linearity]
+
+
+
+# ---------------------------------------------------------------- sparse top-k pins
+def _sparse_brute(q_bits, rows_per_seq, seqlens, indices, dv, scale, h_kv):
+    qf = f64_of(q_bits)
+    b, s_q, h_q, d = qf.shape
+    o = np.zeros((b, s_q, h_q, dv))
+    lse = np.zeros((b, s_q, h_q))
+    for bi in range(b):
+        kf = f64_of(rows_per_seq[bi])                      # [T, h_kv, d]
+        for i in range(s_q):
+            sel = [int(j) for j in indices[bi, i] if 0 <= j < seqlens[bi]]
+            for h in range(h_q):
+                g = h // (h_q // h_kv)
+                if not sel:
+                    lse[bi, i, h] = -math.inf
+                    continue
+                K = kf[sel, g, :]                          # repeats kept
+                e = np.exp(scale * (K @ qf[bi, i, h]))
+                o[bi, i, h] = (e @ K[:, :dv]) / e.sum()
+                lse[bi, i, h] = math.log(e.sum())
+    return o, lse
+
+
+def _random_lists(rng, seqlens, s_q, topk):
+    """Lists mixing valid positions, repeats, -1 padding and positions >= T."""
+    lists = np.full((len(seqlens), s_q, topk), -1, np.int32)
+    for b, T in enumerate(seqlens):
+        for i in range(s_q):
+            n = int(rng.integers(0, topk + 1))
+            vals = rng.integers(-1, T + 2, size=n) if T > 0 else rng.integers(-1, 3, size=n)
+            lists[b, i, :n] = vals
+            if T > 0 and n >= 2:
+                lists[b, i, 1] = lists[b, i, 0] if lists[b, i, 0] >= 0 else T - 1   # a repeat
+            if n >= 3:
+                lists[b, i, 2] = T                                               # one past the end
+    return lists
+
+
+def pin_sparse_brute_force(decode, decode_sparse, seed=31):
+    rng = np.random.default_rng(seed)
+    cases = [
+        # (b, s_q, h_q, h_kv, seqlens, topk, d, dv, page)
+        (2, 1, 16, 1, [100, 37], 48, 576, 512, 64),
+        (3, 2, 4, 1, [1, 200, 0], 70, 576, 512, 64),
+        (2, 3, 8, 2, [130, 65], 33, 512, 512, 64),
+        (1, 4, 2, 1, [9], 12, 40, 24, 4),
+    ]
+    for (b, s_q, h_q, h_kv, seqlens, topk, d, dv, page) in cases:
+        q = rand_bits(rng, (b, s_q, h_q, d))
+        rows = [rand_bits(rng, (max(T, 1), h_kv, d)) for T in seqlens]
+        kc, bt = page_out(rows, page, rng)
+        idx = _random_lists(rng, seqlens, s_q, topk)
+        scale = 1.0 / math.sqrt(d)
+        sl = np.array(seqlens, np.int32)
+        o, lse = decode_sparse(q, kc, bt, sl, idx, dv, scale)
+        o_ref, lse_ref = _sparse_brute(q, rows, seqlens, idx, dv, scale, h_kv)
+        assert np.array_equal(np.isneginf(lse), np.isneginf(lse_ref)), "rows without valid entries differ"
+        fin = ~np.isneginf(lse_ref)
+        assert np.allclose(lse[fin], lse_ref[fin], rtol=0, atol=1e-11), "sparse LSE differs from brute force"
+        assert np.allclose(o, o_ref, rtol=1e-11, atol=1e-12), "sparse O differs from brute force"
+
+
+def pin_sparse_full_list(decode, decode_sparse, seed=32):
+    rng = np.random.default_rng(seed)
+    d, dv, page = 576, 512, 64
+    seqlens = [150, 64, 1]
+    q = rand_bits(rng, (3, 1, 8, d))
+    kc, bt = page_out([rand_bits(rng, (T, 1, d)) for T in seqlens], page, rng)
+    sl = np.array(seqlens, np.int32)
+    idx = np.full((3, 1, 160), -1, np.int32)
+    for b, T in enumerate(seqlens):
+        idx[b, 0, :T] = np.arange(T)
+    o, lse = decode_sparse(q, kc, bt, sl, idx, dv, 1.0 / 24)
+    o_d, lse_d = decode(q, kc, bt, sl, dv, 1.0 / 24, False)
+    assert np.array_equal(lse, lse_d) and np.array_equal(o, o_d), "the full list must give the dense decode"
+
+
+def pin_sparse_order(decode, decode_sparse, seed=33):
+    rng = np.random.default_rng(seed)
+    d, dv, page = 576, 512, 64
+    seqlens = [300, 90]
+    q = rand_bits(rng, (2, 2, 4, d))
+    kc, bt = page_out([rand_bits(rng, (T, 1, d)) for T in seqlens], page, rng)
+    sl = np.array(seqlens, np.int32)
+    idx = np.stack([np.stack([rng.choice(T, size=40, replace=False) for _ in range(2)]) for T in seqlens]).astype(
+        np.int32)
+    o, lse = decode_sparse(q, kc, bt, sl, idx, dv, 1.0 / 24)
+    perm = idx[:, :, rng.permutation(40)]
+    o_p, lse_p = decode_sparse(q, kc, bt, sl, perm, dv, 1.0 / 24)
+    assert np.allclose(lse_p, lse, rtol=0, atol=1e-12) and np.allclose(o_p, o, rtol=1e-12, atol=1e-14), \
+        "the order of a list must not matter"
+    padded = np.concatenate([idx, np.full((2, 2, 3), -1, np.int32), np.stack([sl, sl], axis=1)[:, :, None]], axis=2)
+    o_x, lse_x = decode_sparse(q, kc, bt, sl, padded, dv, 1.0 / 24)
+    assert np.array_equal(lse_x, lse) and np.array_equal(o_x, o), "ignored entries must change nothing"
+
+
+SPARSE_PINS = [pin_sparse_brute_force, pin_sparse_full_list, pin_sparse_order]

@@ -25,6 +25,11 @@ def test_oracle_fp8_pin(pin):
     pin(oracle.mla_decode, oracle.mla_decode_fp8, oracle.e4m3_to_float64)
 
 
+@pytest.mark.parametrize("pin", pins.SPARSE_PINS, ids=lambda p: p.__name__)
+def test_oracle_sparse_pin(pin):
+    pin(oracle.mla_decode, oracle.mla_decode_sparse)
+
+
 # (description, text in mla_oracle.c, replacement)
 MUTANTS = [
     ("scale dropped", "scores[j] = scale * acc;", "scores[j] = acc;"),
@@ -43,10 +48,16 @@ MUTANTS = [
     ("scale of the neighbouring token", "+ 4 * t, sizeof sc)", "+ 4 * ((t + 1) % page), sizeof sc)"),
     ("scale left out", "row[c] = (double)sc * oracle_e4m3_to_double(", "row[c] = oracle_e4m3_to_double("),
     ("page stride without the scales", "blk * ((int64_t)page * d + (int64_t)page * 4)", "blk * ((int64_t)page * d)"),
+    # the sparse top-k decode
+    ("one-past-the-end entry kept", "if (list[t] >= 0 && list[t] < T) keys[n++]", "if (list[t] >= 0 && list[t] <= T) keys[n++]"),
+    ("first list entry skipped", "for (int t = 0; t < topk; ++t)\n        if (list[t]", "for (int t = 1; t < topk; ++t)\n        if (list[t]"),
+    ("list of the wrong query token", "indices + (b * s_q + i) * (int64_t)topk", "indices + (b * s_q) * (int64_t)topk"),
+    ("repeats dropped", "if (list[t] >= 0 && list[t] < T) keys[n++] = list[t];",
+     "if (list[t] >= 0 && list[t] < T && (n == 0 || keys[n - 1] != list[t])) keys[n++] = list[t];"),
 ]
 
 
-def _all_pins_pass(decode, decode_fp8, e4m3):
+def _all_pins_pass(decode, decode_fp8, e4m3, decode_sparse):
     for pin in pins.ALL_PINS:
         try:
             pin(decode)
@@ -55,6 +66,11 @@ def _all_pins_pass(decode, decode_fp8, e4m3):
     for pin in pins.FP8_PINS:
         try:
             pin(decode, decode_fp8, e4m3)
+        except (AssertionError, ValueError):
+            return False
+    for pin in pins.SPARSE_PINS:
+        try:
+            pin(decode, decode_sparse)
         except (AssertionError, ValueError):
             return False
     return True
@@ -83,4 +99,8 @@ def test_pins_catch_planted_mistake(mutant):
         def e4m3(codes):
             return oracle.e4m3_to_float64(codes, lib=lib)
 
-        assert not _all_pins_pass(decode, decode_fp8, e4m3), f"no pin caught the planted mistake: {desc}"
+        def decode_sparse(*args, **kw):
+            return oracle.mla_decode_sparse(*args, lib=lib, **kw)
+
+        assert not _all_pins_pass(decode, decode_fp8, e4m3, decode_sparse), \
+            f"no pin caught the planted mistake: {desc}"
