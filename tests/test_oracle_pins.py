@@ -104,3 +104,21 @@ def test_pins_catch_planted_mistake(mutant):
 
         assert not _all_pins_pass(decode, decode_fp8, e4m3, decode_sparse), \
             f"no pin caught the planted mistake: {desc}"
+
+
+def test_e4m3_page_generator_round_trips():
+    # the seeded e4m3 pages (input generation, shared by both sides) hold each
+    # token's rows to within e4m3 rounding (relative 2^-4 of the row's max |k|)
+    import torch
+    from mla_decode_attention_latent_gb300 import workloads as W
+    rows = torch.randn((3, 64, 576), generator=torch.Generator().manual_seed(5)) * 3.0
+    rows[1, 7] = 0.0                                   # an all-zero row keeps scale 1
+    pages = W.pack_e4m3_pages(rows)
+    assert pages.shape == (3, 64 * 576 + 256) and pages.dtype == torch.uint8
+    codes, scales = W.e4m3_page_codes(pages)
+    deq = oracle.e4m3_to_float64(codes.numpy()) * scales.double().numpy()[..., None]
+    amax = rows.abs().amax(dim=-1, keepdim=True).double().numpy()
+    assert abs(float(scales[1, 7]) - 1.0) == 0.0 and not deq[1, 7].any()
+    assert (abs(deq - rows.double().numpy()) <= amax * 2.0 ** -4 + 1e-30).all()
+    nz = amax[..., 0] > 0                              # other rows: scale = max |k| / 448
+    assert abs(scales.double().numpy()[nz] * 448.0 - amax[..., 0][nz]).max() <= 1e-4 * amax.max()
