@@ -315,3 +315,13 @@ def test_fp8_deterministic_and_split_invariant():
         o2, l2, *_ = run_gpu(x, num_parts=p)
         assert torch.allclose(o1.float(), o2.float(), rtol=1e-2, atol=2e-3)
         assert torch.allclose(l1, l2, atol=1e-4)
+
+
+@pytest.mark.parametrize("batch,s_q,h_q,seqlens", [
+    (2, 64, 128, [700, 130]),     # 64 query tokens x 128 heads: 64 row tiles per sequence
+    (1, 256, 16, [1000]),         # a 256-token causal chunk over a 744-token prefix (prefill-like)
+])
+def test_large_q_len(batch, s_q, h_q, seqlens):
+    # many query tokens per step, causal: each row sees T - s_q + i + 1 keys,
+    # and a 128-row tile holds 128 / h_q query tokens with different windows
+    check(case(f"q{s_q}", batch, s_q, h_q, seqlens, causal=True, seed=140 + s_q))
