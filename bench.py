@@ -116,12 +116,37 @@ def split_kernel_traffic(workload):
 
 
 def split_source_hash():
+    """sha256 of the split kernel's sources with comments and blank space removed
+    (a comment edit leaves the compiled kernel, and so its counters, unchanged)."""
     csrc = os.path.join(ROOT, "mla_decode_attention_latent_gb300", "csrc")
     hs = hashlib.sha256()
     for name in sorted(os.listdir(csrc)):
         if name.startswith("mla_split") or name.endswith((".cuh", ".h")):
-            hs.update(open(os.path.join(csrc, name), "rb").read())
+            hs.update(_code_only(open(os.path.join(csrc, name)).read()).encode())
     return hs.hexdigest()
+
+
+def _code_only(src):
+    """C/C++ source without // and /* */ comments (string literals kept) or blank space."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"' or c == "'":                       # a literal: copy through its closing quote
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            i = src.find("\n", i)
+            i = n if i < 0 else i
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "".join("".join(out).split())
 
 
 # ------------------------------------------------------------------ clocks

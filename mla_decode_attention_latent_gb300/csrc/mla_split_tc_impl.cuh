@@ -52,13 +52,14 @@
 //
 // e4m3 cache (MLA_SPLIT_FP8 = 1, D = 576): a page holds 64 rows of e4m3 codes
 // followed by 64 fp32 per-token scales, and row j dequantizes to c_j * code_j
-// (include/mla_decode.h).  The loads land in the upper half of the same K slots
-// and V stages, and are widened in place to f16 (exact for every e4m3 value):
-// in the score CTA by the whole warp of each TMA producer, in the value CTA by
-// its row warps, which also zero the rows past a sequence's end.  Both MMAs
-// then run in f16 (Q and P rounded to f16).  A token's scale multiplies its
-// score column before the softmax and its P column before P V, so the
-// accumulators see c_j * code_j exactly as the dequantized row.
+// (include/mla_decode.h).  The codes are widened to f16 (exact for every e4m3
+// value) in shared memory: in the score CTA by the whole warp of each TMA
+// producer, from a ring of landing buffers into the MMA operand slots; in the
+// value CTA by its row warps, in place in the upper half of each V stage, also
+// zeroing the rows past a sequence's end.  Both MMAs then run in f16 (Q and P
+// rounded to f16).  A token's scale multiplies its score column before the
+// softmax and its P column before P V, so the accumulators see c_j * code_j
+// exactly as the dequantized row.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -128,7 +129,8 @@ constexpr uint32_t kScBytes = 2 * kPage * 4;               // 512 B
 static_assert(kE4PageBytes % 16 == 0 && kE4ScaleOff % 16 == 0, "TMA and bulk-copy alignment of e4m3 pages");
 
 // shared-memory layout (offsets from the 1024-byte aligned base)
-// score CTA: [K rings 2 x 5 x 16 KB][Q RoPE tile 16 KB][P staging 2 x 17 KB]
+// score CTA: [K operand rings 2 x 5 x 16 KB][Q RoPE tile 16 KB][P staging 2 x 17 KB];
+// e4m3: [operand rings 2 x 2 x 16 KB][landing rings 2 x 6 x 8 KB][Q RoPE][P staging][scales 8 x 512 B]
 constexpr uint32_t kKRingOff = 0;
 constexpr uint32_t kLandOff = kKRingOff + kKSlots * kSlotBytes;  // e4m3: the landing rings
 constexpr uint32_t kQRopeOff = kLandOff + (kFp8 ? kScoreIssuers * kLandSlots * kLandBytes : 0);
