@@ -223,6 +223,44 @@ MLA_API int mla_decode_kvcache_fp8(const void *q, const void *kv_pages, int64_t 
                                    size_t workspace_bytes, struct CUstream_st *stream);
 
 /*
+ * mla_decode_kvcache_sparse — sparse top-k decode: each query token attends
+ * only to the cached tokens its index list names.
+ *
+ * The page "[flashinfer] FlashInfer, SM120 GPU를 위한 희소 MLA 커널 추가로 LLM
+ * 추론 속도 향상" (section "왜 이게 좋은가?", item 2) describes sparse MLA as
+ * attention over only the top-k selected tokens of a paged cache; it gives no
+ * interface.  This library's reading: query token i of sequence b carries
+ * indices[b][i][0 .. topk) (token positions, shared by all its heads); an
+ * entry is ignored when it is outside [0, cache_seqlens[b]) (-1 pads short
+ * lists) or at or past list_lens[b]; every other entry is one term of the
+ * softmax (a position listed twice counts twice); no causal mask applies:
+ *   s_t = softmax_scale * <q, k_{indices[t]}>,  lse = ln sum_t exp(s_t),
+ *   o   = sum_t exp(s_t - lse) * k_{indices[t]}[0..512)   over valid entries t.
+ * A row with no valid entry gets o = 0 and lse = -inf.
+ *
+ *   kcache, block_table, cache_seqlens, q, o, lse, workspace
+ *                  as for mla_decode_kvcache (bf16 cache, d = 576 only)
+ *   indices        device int32 [batch][s_q][topk]
+ *   topk           entries per list, >= 1
+ *   list_lens      device int32 [batch]: the lengths the work partition was
+ *                  computed on (tile_scheduler_metadata and num_splits come
+ *                  from mla_get_metadata on this array; normally topk for
+ *                  every sequence)
+ * A 128-row tile holds one query token's heads: s_q must be 1, or h_q 128
+ * (MLA_ERR_UNSUPPORTED otherwise).  Rows are gathered one by one from the
+ * cache, so any positions may be listed.
+ * Stream order, graph capture and errors: as for mla_decode_kvcache.
+ */
+MLA_API int mla_decode_kvcache_sparse(const void *q, const void *kcache, int64_t num_blocks,
+                                      const int32_t *block_table, int max_blocks_per_seq,
+                                      const int32_t *cache_seqlens, const int32_t *indices, int topk,
+                                      const int32_t *list_lens, int batch, int s_q, int h_q, int h_kv,
+                                      int d, int dv, const int32_t *tile_scheduler_metadata,
+                                      const int32_t *num_splits, int num_parts, float softmax_scale,
+                                      void *o, float *lse, void *workspace, size_t workspace_bytes,
+                                      struct CUstream_st *stream);
+
+/*
  * mla_decode_kvcache_noalloc — mla_decode_kvcache for callers that cannot
  * allocate device memory.
  *

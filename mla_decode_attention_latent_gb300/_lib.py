@@ -46,6 +46,8 @@ SIGNATURES = {
                                 _P, _SZ, _P]),
     "mla_decode_kvcache_fp8": (_I, [_P, _P, _I64, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _F, _I, _P, _P,
                                     _P, _SZ, _P]),
+    "mla_decode_kvcache_sparse": (_I, [_P, _P, _I64, _P, _I, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _F,
+                                       _P, _P, _P, _SZ, _P]),
     "mla_decode_kvcache_noalloc": (_I, [_P, _P, _I64, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _F, _I, _P,
                                         _P, _P]),
     "mla_device_status": (_I, [ctypes.POINTER(ctypes.c_int), _I]),

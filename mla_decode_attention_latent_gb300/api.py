@@ -173,6 +173,60 @@ def mla_decode_kvcache_fp8(q: torch.Tensor, kv_pages: torch.Tensor, block_table:
     return out, lse
 
 
+def mla_decode_kvcache_sparse(q: torch.Tensor, kcache: torch.Tensor, block_table: torch.Tensor,
+                              cache_seqlens: torch.Tensor, indices: torch.Tensor, dv: int,
+                              tile_scheduler_metadata: Optional[torch.Tensor] = None,
+                              num_splits: Optional[torch.Tensor] = None, list_lens: Optional[torch.Tensor] = None,
+                              softmax_scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                              lse: Optional[torch.Tensor] = None,
+                              workspace: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Sparse top-k MLA decode: query token i of sequence b attends to the cache
+    positions ``indices[b, i]`` (int32 [b, s_q, topk]; entries outside
+    [0, cache_seqlens[b]) are ignored).  The work partition is computed on
+    ``list_lens`` (default: topk for every sequence) unless given.  Returns
+    (o bf16 [b, s_q, h_q, dv], lse fp32 [b, s_q, h_q]); see ``include/mla_decode.h``."""
+    for name, t, dt in (("q", q, torch.bfloat16), ("kcache", kcache, torch.bfloat16),
+                        ("block_table", block_table, torch.int32), ("cache_seqlens", cache_seqlens, torch.int32),
+                        ("indices", indices, torch.int32)):
+        _need_cuda(name, t, dt)
+    if q.dim() != 4 or kcache.dim() != 4 or indices.dim() != 3:
+        raise ValueError("q must be [b, s_q, h_q, d], kcache [num_blocks, page, h_kv, d], indices [b, s_q, topk]")
+    b, s_q, h_q, d = q.shape
+    num_blocks, page, h_kv, dk = kcache.shape
+    if dk != d or page != _lib.MLA_PAGE_SIZE or tuple(indices.shape[:2]) != (b, s_q):
+        raise ValueError("kcache and indices must match q")
+    topk = indices.shape[2]
+    dev = q.device
+    if list_lens is None:
+        list_lens = torch.full((b,), topk, dtype=torch.int32, device=dev)
+    _need_cuda("list_lens", list_lens, torch.int32)
+    if tile_scheduler_metadata is None or num_splits is None:
+        tile_scheduler_metadata, num_splits = mla_get_metadata(list_lens, s_q * h_q // h_kv, h_kv)
+    _need_cuda("tile_scheduler_metadata", tile_scheduler_metadata, torch.int32)
+    _need_cuda("num_splits", num_splits, torch.int32)
+    num_parts = tile_scheduler_metadata.shape[0]
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((b, s_q, h_q, dv), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((b, s_q, h_q), dtype=torch.float32, device=dev)
+    _need_cuda("out", out, torch.bfloat16)
+    _need_cuda("lse", lse, torch.float32)
+    ws_need = mla_workspace_bytes(b, s_q, h_q, h_kv, dv, num_parts) if dv == MLA_V_DIM and h_q % h_kv == 0 else 256
+    if workspace is None:
+        workspace = torch.empty((ws_need,), dtype=torch.uint8, device=dev)
+    _need_cuda("workspace", workspace, torch.uint8)
+    with torch.cuda.device(dev):
+        st = load().mla_decode_kvcache_sparse(
+            q.data_ptr(), kcache.data_ptr(), num_blocks, block_table.data_ptr(), block_table.shape[1],
+            cache_seqlens.data_ptr(), indices.data_ptr(), topk, list_lens.data_ptr(), b, s_q, h_q, h_kv, d, dv,
+            tile_scheduler_metadata.data_ptr(), num_splits.data_ptr(), num_parts, float(softmax_scale),
+            out.data_ptr(), lse.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream_handle(dev))
+    check("mla_decode_kvcache_sparse", st)
+    return out, lse
+
+
 def mla_decode_kvcache_noalloc(q: torch.Tensor, kcache: torch.Tensor, block_table: torch.Tensor,
                                cache_seqlens: torch.Tensor, dv: int, tile_scheduler_metadata: torch.Tensor,
                                num_splits: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,

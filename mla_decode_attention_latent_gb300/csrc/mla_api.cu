@@ -103,11 +103,22 @@ size_t mla_workspace_bytes(int batch, int s_q, int h_q, int h_kv, int dv, int nu
 
 namespace {
 
-// The decode behind both cache formats: validation, then split + combine.
-int decode(const void *q, const void *kcache, bool e4m3, int64_t num_blocks, const int32_t *block_table,
+enum class Kind { kBf16, kE4m3, kSparse };
+
+// Index lists of the sparse decode (unused otherwise).
+struct Lists {
+    const int32_t *indices = nullptr;  // [batch][s_q][topk]
+    int topk = 0;
+    const int32_t *list_lens = nullptr;  // [batch]: the lengths the work partition was computed on
+};
+
+// The decode behind every cache format: validation, then split + combine.
+int decode(const void *q, const void *kcache, Kind kind, int64_t num_blocks, const int32_t *block_table,
            int max_blocks_per_seq, const int32_t *cache_seqlens, int batch, int s_q, int h_q, int h_kv, int d, int dv,
            const int32_t *tile_scheduler_metadata, const int32_t *num_splits, int num_parts, float softmax_scale,
-           int causal, void *o, float *lse, void *workspace, size_t ws_bytes, struct CUstream_st *stream) {
+           int causal, void *o, float *lse, void *workspace, size_t ws_bytes, struct CUstream_st *stream,
+           const Lists &lists = Lists()) {
+    const bool e4m3 = kind == Kind::kE4m3, sparse = kind == Kind::kSparse;
     if (!q || !kcache || !block_table || !cache_seqlens || !tile_scheduler_metadata || !num_splits || !o || !lse ||
         !workspace)
         return MLA_ERR_INVALID_ARG;
@@ -117,6 +128,11 @@ int decode(const void *q, const void *kcache, bool e4m3, int64_t num_blocks, con
     if (!(softmax_scale == softmax_scale)) return MLA_ERR_INVALID_ARG;
     if ((d != kDqk && d != kDv) || dv != kDv || h_kv != 1) return MLA_ERR_UNSUPPORTED;
     if (e4m3 && d != kDqk) return MLA_ERR_UNSUPPORTED;
+    if (sparse) {
+        if (!lists.indices || !lists.list_lens || lists.topk < 1) return MLA_ERR_INVALID_ARG;
+        // a 128-row tile must hold the heads of one query token
+        if (d != kDqk || (s_q > 1 && h_q != kRowsPerTile)) return MLA_ERR_UNSUPPORTED;
+    }
     if ((long long)s_q * h_q > kMaxRows) return MLA_ERR_UNSUPPORTED;
     if ((long long)max_blocks_per_seq * kPage > 0x7fffffffLL) return MLA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(kcache) || !aligned16(o) || !aligned16(workspace)) return MLA_ERR_INVALID_ARG;
@@ -129,7 +145,7 @@ int decode(const void *q, const void *kcache, bool e4m3, int64_t num_blocks, con
     p.num_blocks = num_blocks;
     p.block_table = block_table;
     p.max_blocks = max_blocks_per_seq;
-    p.seqlens = cache_seqlens;
+    p.seqlens = sparse ? lists.list_lens : cache_seqlens;
     p.batch = batch;
     p.s_q = s_q;
     p.h_q = h_q;
@@ -139,7 +155,10 @@ int decode(const void *q, const void *kcache, bool e4m3, int64_t num_blocks, con
     p.num_parts = num_parts;
     p.max_splits = batch + num_parts;
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
-    p.causal = (causal != 0 && s_q > 1) ? 1 : 0;
+    p.causal = (causal != 0 && s_q > 1 && !sparse) ? 1 : 0;
+    p.indices = lists.indices;
+    p.topk = lists.topk;
+    p.kv_lens = cache_seqlens;
     p.o = static_cast<uint16_t *>(o);
     p.lse = lse;
     carve_workspace(workspace, batch, rows, num_parts, &p.o_accum, &p.lse_accum);
@@ -153,8 +172,9 @@ int decode(const void *q, const void *kcache, bool e4m3, int64_t num_blocks, con
         ev_end = g_split_end;
     }
     if (ev_begin && cudaEventRecord(ev_begin, s) != cudaSuccess) return MLA_ERR_CUDA;
-    cudaError_t e = e4m3 ? launch_split_kv_tc<576, true>(p, s)
-                         : (d == kDqk ? launch_split_kv_tc<576, false>(p, s) : launch_split_kv_tc<512, false>(p, s));
+    cudaError_t e = sparse ? launch_split_kv_tc_sparse(p, s)
+                    : e4m3 ? launch_split_kv_tc<576, true>(p, s)
+                           : (d == kDqk ? launch_split_kv_tc<576, false>(p, s) : launch_split_kv_tc<512, false>(p, s));
     if (e != cudaSuccess) return MLA_ERR_CUDA;
     if (ev_end && cudaEventRecord(ev_end, s) != cudaSuccess) return MLA_ERR_CUDA;
     e = launch_combine(p, s);
@@ -170,7 +190,7 @@ int mla_decode_kvcache(const void *q, const void *kcache, int64_t num_blocks, co
                        int h_kv, int d, int dv, const int32_t *tile_scheduler_metadata,
                        const int32_t *num_splits, int num_parts, float softmax_scale, int causal, void *o,
                        float *lse, void *workspace, size_t ws_bytes, struct CUstream_st *stream) {
-    return decode(q, kcache, false, num_blocks, block_table, max_blocks_per_seq, cache_seqlens, batch, s_q, h_q, h_kv,
+    return decode(q, kcache, Kind::kBf16, num_blocks, block_table, max_blocks_per_seq, cache_seqlens, batch, s_q, h_q, h_kv,
                   d, dv, tile_scheduler_metadata, num_splits, num_parts, softmax_scale, causal, o, lse, workspace,
                   ws_bytes, stream);
 }
@@ -180,9 +200,24 @@ int mla_decode_kvcache_fp8(const void *q, const void *kv_pages, int64_t num_bloc
                            int h_kv, int d, int dv, const int32_t *tile_scheduler_metadata,
                            const int32_t *num_splits, int num_parts, float softmax_scale, int causal, void *o,
                            float *lse, void *workspace, size_t ws_bytes, struct CUstream_st *stream) {
-    return decode(q, kv_pages, true, num_blocks, block_table, max_blocks_per_seq, cache_seqlens, batch, s_q, h_q, h_kv,
+    return decode(q, kv_pages, Kind::kE4m3, num_blocks, block_table, max_blocks_per_seq, cache_seqlens, batch, s_q, h_q, h_kv,
                   d, dv, tile_scheduler_metadata, num_splits, num_parts, softmax_scale, causal, o, lse, workspace,
                   ws_bytes, stream);
+}
+
+int mla_decode_kvcache_sparse(const void *q, const void *kcache, int64_t num_blocks, const int32_t *block_table,
+                              int max_blocks_per_seq, const int32_t *cache_seqlens, const int32_t *indices, int topk,
+                              const int32_t *list_lens, int batch, int s_q, int h_q, int h_kv, int d, int dv,
+                              const int32_t *tile_scheduler_metadata, const int32_t *num_splits, int num_parts,
+                              float softmax_scale, void *o, float *lse, void *workspace, size_t ws_bytes,
+                              struct CUstream_st *stream) {
+    Lists lists;
+    lists.indices = indices;
+    lists.topk = topk;
+    lists.list_lens = list_lens;
+    return decode(q, kcache, Kind::kSparse, num_blocks, block_table, max_blocks_per_seq, cache_seqlens, batch, s_q,
+                  h_q, h_kv, d, dv, tile_scheduler_metadata, num_splits, num_parts, softmax_scale, 0, o, lse,
+                  workspace, ws_bytes, stream, lists);
 }
 
 int mla_device_status(int *status, int clear) {

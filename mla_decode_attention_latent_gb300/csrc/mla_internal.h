@@ -38,6 +38,10 @@ struct DecodeParams {
     float *o_accum;               // [max_splits][rows][512] fp32 partial outputs
     float *lse_accum;             // [max_splits][rows] partial LSE (natural log)
     unsigned int *status;         // device status word (MLA_DEVERR_* bits)
+    // sparse top-k decode only (seqlens then holds each sequence's list length)
+    const int32_t *indices;       // [batch][s_q][topk] token positions per query token
+    int topk;
+    const int32_t *kv_lens;       // [batch] cache lengths: positions >= kv_lens[b] are ignored
 };
 
 // Workspace carve-up shared by the API, the split kernel and the combine.
@@ -50,6 +54,8 @@ cudaError_t launch_schedule(const int32_t *seqlens, int batch, int num_parts, in
 // rows or (E4M3, D = 576) packed e4m3 pages with per-token scales
 template <int D, bool E4M3>
 cudaError_t launch_split_kv_tc(const DecodeParams &p, cudaStream_t stream);
+// the sparse top-k variant (576-wide bf16 rows gathered from index lists)
+cudaError_t launch_split_kv_tc_sparse(const DecodeParams &p, cudaStream_t stream);
 int split_kv_tc_tile_rows();
 // CTA pairs of the split-KV kernel that fit on the current device at once
 template <int D, bool E4M3>

@@ -182,6 +182,22 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
                  : "memory");
 }
 
+// 16-byte asynchronous copy global -> this CTA's shared memory (cp.async,
+// cached in L2 only); src_bytes = 0 writes 16 zero bytes and reads nothing.
+// Both addresses 16-byte aligned.  Completion: cp_async_commit / cp_async_wait.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)),
+                 "r"(src_bytes)
+                 : "memory");
+}
+// close this thread's group of cp.async copies
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// wait until at most N of this thread's most recent groups are still in flight
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // prefetch a contiguous global range into L2
 // bring the line holding `src` into L1 (no register result, never faults)
 __device__ __forceinline__ void prefetch_line_l1(const void *src) {

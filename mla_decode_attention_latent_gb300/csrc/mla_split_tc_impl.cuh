@@ -86,6 +86,12 @@ constexpr bool kHasRope = kD > kDv;            // a RoPE part beyond the value d
 #define MLA_SPLIT_FP8 0
 #endif
 constexpr bool kFp8 = MLA_SPLIT_FP8 != 0;      // e4m3 cache pages with per-token scales
+#ifndef MLA_SPLIT_SPARSE
+#define MLA_SPLIT_SPARSE 0
+#endif
+constexpr bool kSparse = MLA_SPLIT_SPARSE != 0;  // keys gathered row by row from per-query-token index lists
+static_assert(!(kSparse && kFp8) && (!kSparse || MLA_SPLIT_D == 576), "sparse decode: 576-wide bf16 rows");
+constexpr bool kRing = kFp8 || kSparse;          // a per-step side ring (e4m3: token scales; sparse: key masks)
 
 constexpr int kThreads = 256;                  // 8 warps: TMA, MMA, 4 row warps, second score MMA issuer and TMA producer
 constexpr int kTileRows = 128;                 // query rows per tile = TMEM lanes
@@ -136,7 +142,7 @@ constexpr uint32_t kLandOff = kKRingOff + kKSlots * kSlotBytes;  // e4m3: the la
 constexpr uint32_t kQRopeOff = kLandOff + (kFp8 ? kScoreIssuers * kLandSlots * kLandBytes : 0);
 constexpr uint32_t kStageOff = kQRopeOff + (kHasRope ? kTileRows * 128 : 0);
 constexpr uint32_t kScaleOff = kStageOff + kPBufs * kPMsgBytes;   // e4m3: per-token scales of the steps in flight
-constexpr uint32_t kScoreEnd = kScaleOff + (kFp8 ? kScSlots * kScBytes : 0);
+constexpr uint32_t kScoreEnd = kScaleOff + (kRing ? kScSlots * kScBytes : 0);
 // value CTA: [V ring 2 x 64 KB][P landing 2 x 17 KB][epilogue staging 34 KB]
 constexpr uint32_t kVRingOff = 0;
 constexpr uint32_t kPBufOff = kVRingOff + kVStages * kVStageBytes;
@@ -161,7 +167,7 @@ enum Bar {
 // B_KFULL / B_VFULL), and the scale ring of the score CTA
 constexpr int B_KLAND = B_BASE_COUNT, B_VLAND = B_KLAND + kScoreIssuers * kLandSlots, B_SCFULL = B_VLAND + kVStages,
               B_SCEMPTY = B_SCFULL + kScSlots, B_VREAD = B_SCEMPTY + kScSlots;
-constexpr int B_COUNT = kFp8 ? B_VREAD + 1 : B_BASE_COUNT;
+constexpr int B_COUNT = kRing ? B_VREAD + 1 : B_BASE_COUNT;
 constexpr uint32_t kTmemSlotOff = kBarOff + B_COUNT * 8;
 constexpr uint32_t kAbortOff = kTmemSlotOff + 4;
 constexpr uint32_t kSmemUsed = kAbortOff + 4;
@@ -188,9 +194,9 @@ struct PartWalk {
     }
     __device__ bool next(const DecodeParams &p, Segment &s) {
         if (b >= p.batch || b > eb || (b == eb && ep == 0)) return false;
-        int T = p.seqlens[b];
+        int T = p.seqlens[b];  // sparse decode: the length of the sequence's lists
         if (T < 0) T = 0;
-        if (T > p.max_blocks * kPage) T = p.max_blocks * kPage;
+        if (!kSparse && T > p.max_blocks * kPage) T = p.max_blocks * kPage;
         s.b = b;
         s.T = T;
         s.n_pages = (T + kPage - 1) / kPage;
@@ -461,6 +467,170 @@ __device__ void score_producer_e4m3(const DecodeParams &p, const Ctx &c, const C
     __syncwarp();
 }
 
+// -------------------------------------------------------------- sparse top-k gathers
+// A part walks list chunks instead of pages: "page" pg of sequence b is list
+// entries 64 pg .. 64 pg + 63 of the tile's query token, and entry e names a
+// token position; positions outside [0, kv_lens[b]) and entries past the
+// list's length are invalid.  Row t of a 64-entry chunk is gathered from the
+// cache row of its position with 16-byte cp.async copies written straight
+// into the 128-byte-swizzled operand layout; an invalid row is zero-filled
+// (its score column is masked by the row warps, its V row contributes 0).
+
+// the cache row of list entry e (or nullptr when the entry is invalid)
+__device__ __forceinline__ const uint8_t *sparse_row(const DecodeParams &p, const int32_t *list, int list_len, int T,
+                                                     int b, int e) {
+    if (e >= list_len) return nullptr;
+    const int pos = list[e];
+    if (pos < 0 || pos >= T) return nullptr;
+    const int blk = p.block_table[(size_t)b * p.max_blocks + pos / kPage];
+    if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+        atomicOr(p.status, MLA_DEVERR_BLOCK_ID);
+        return nullptr;
+    }
+    return reinterpret_cast<const uint8_t *>(p.kcache) + ((size_t)blk * kPage + pos % kPage) * (kD * 2);
+}
+
+__device__ __forceinline__ int sparse_cache_len(const DecodeParams &p, int b) {
+    int T = p.kv_lens[b];
+    return T < 0 ? 0 : (T > p.max_blocks * kPage ? p.max_blocks * kPage : T);
+}
+
+// Score-CTA producer of the sparse decode; the whole warp runs it.  Lane l
+// gathers rows l, l + 32 (first list chunk of the step) and l + 64, l + 96
+// (second), 8 copies per row and 64-dim chunk; each chunk's copies are one
+// cp.async group, handed to the MMA issuer (B_KFULL) once complete, kGatherLag
+// chunks later.  The validity masks of the step's two list chunks go to the
+// side ring for the row warps.
+constexpr int kGatherLag = 4;
+static_assert(!kSparse || kGatherLag < kRingSlots, "a chunk is handed over before its slot is needed again");
+__device__ void score_producer_sparse(const DecodeParams &p, const Ctx &c, int part, int tile, int r) {
+    const int lane = threadIdx.x & 31;
+    const int qtok = p.s_q == 1 ? 0 : tile;  // the tile's query token (h_q = 128 when s_q > 1)
+    PartWalk walk;
+    Segment s;
+    if (lane == 0 && r == 0) {
+        const int rows = min(kTileRows, p.rows - tile * kTileRows);
+        walk.init(p, part);
+        while (walk.next(p, s))
+            if (s.p1 > s.p0 && rows > 0)
+                prefetch_l2(p.q + ((size_t)s.b * p.rows + (size_t)tile * kTileRows) * kD, (uint32_t)rows * kD * 2);
+    }
+    auto hand_over = [&](uint32_t k) {
+        fence_proxy_async_smem();  // this lane's completed copies, before the MMA's reads
+        __syncwarp();
+        if (lane == 0) mbar_arrive(c.bar(B_KFULL + r * kRingSlots + (int)(k % kRingSlots)));
+    };
+    walk.init(p, part);
+    uint32_t issued = 0, step = 0;
+    bool ok = true;
+    while (ok && walk.next(p, s)) {
+        const int T = sparse_cache_len(p, s.b);
+        const int32_t *list = p.indices + ((size_t)s.b * p.s_q + qtok) * p.topk;
+        const int list_len = min(s.T, p.topk);
+        for (int pg = s.p0; ok && pg < s.p1; pg += 2, ++step) {
+            const int npg = min(2, s.p1 - pg);
+            if ((int)(step % kScoreIssuers) != r) continue;  // the other ring's step
+            const uint8_t *src[4];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+                src[q4] = (q4 < 2 || npg > 1) ? sparse_row(p, list, list_len, T, s.b, kPage * pg + 32 * q4 + lane) : nullptr;
+            const uint32_t m0 = __ballot_sync(0xffffffffu, src[0] != nullptr), m1 = __ballot_sync(0xffffffffu, src[1] != nullptr),
+                           m2 = __ballot_sync(0xffffffffu, src[2] != nullptr), m3 = __ballot_sync(0xffffffffu, src[3] != nullptr);
+            const int sc = (int)(step % kScSlots);
+            if (!warp_wait(c, B_SCEMPTY + sc, ((step / kScSlots) & 1) ^ 1)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
+                sts128(smem_u32(c.base + kScaleOff + sc * kScBytes), m0, m1, m2, m3);
+                mbar_arrive(c.bar(B_SCFULL + sc));
+            }
+            for (int ch = 0; ch < kKChunks; ++ch) {
+                const uint32_t k = issued;
+                const int sl = r * kRingSlots + (int)(k % kRingSlots);
+                if (!warp_wait(c, B_KEMPTY + sl, ((k / kRingSlots) & 1) ^ 1)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t slot = smem_u32(c.base + kKRingOff + sl * kSlotBytes);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    if (q4 >= 2 && npg < 2) break;
+                    const int R = 32 * q4 + lane;
+                    const uint32_t row = slot + 128u * (uint32_t)R;
+                    const uint8_t *g = src[q4] ? src[q4] + ch * 128 : reinterpret_cast<const uint8_t *>(p.kcache);
+                    const uint32_t nb = src[q4] ? 16u : 0u;
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) cp_async16(row + 16u * (uint32_t)(cc ^ (R & 7)), g + (src[q4] ? 16 * cc : 0), nb);
+                }
+                cp_async_commit();
+                ++issued;
+                if (k >= (uint32_t)kGatherLag) {
+                    cp_async_wait<kGatherLag>();
+                    hand_over(k - kGatherLag);
+                }
+            }
+        }
+    }
+    cp_async_wait<0>();  // no copy may be in flight when this CTA exits
+    if (ok)
+        for (uint32_t k = issued > (uint32_t)kGatherLag ? issued - kGatherLag : 0; k < issued; ++k) hand_over(k);
+    __syncwarp();
+}
+
+// Value-CTA producer of the sparse decode; the whole warp runs it.  Lane l
+// gathers rows l and l + 32 of each list chunk (dims 0..511: 8 chunks x 8
+// copies per row) into the V stage; a stage is handed over (B_VFULL) once its
+// copies are complete, one page later.
+__device__ void value_producer_sparse(const DecodeParams &p, const Ctx &c, int part, int tile) {
+    const int lane = threadIdx.x & 31;
+    const int qtok = p.s_q == 1 ? 0 : tile;
+    PartWalk walk;
+    Segment s;
+    walk.init(p, part);
+    uint32_t it = 0;
+    bool ok = true;
+    auto hand_over = [&](uint32_t k) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(c.bar(B_VFULL + (int)(k % kVStages)));
+    };
+    while (ok && walk.next(p, s)) {
+        const int T = sparse_cache_len(p, s.b);
+        const int32_t *list = p.indices + ((size_t)s.b * p.s_q + qtok) * p.topk;
+        const int list_len = min(s.T, p.topk);
+        for (int pg = s.p0; pg < s.p1; ++pg, ++it) {
+            const int st = it % kVStages;
+            if (!warp_wait(c, B_VEMPTY + st, ((it / kVStages) & 1) ^ 1)) {
+                ok = false;
+                break;
+            }
+            const uint32_t stage = smem_u32(c.base + kVRingOff + st * kVStageBytes);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int R = 32 * h + lane;
+                const uint8_t *src = sparse_row(p, list, list_len, T, s.b, kPage * pg + R);
+                const uint8_t *g = src ? src : reinterpret_cast<const uint8_t *>(p.kcache);
+                const uint32_t nb = src ? 16u : 0u;
+#pragma unroll
+                for (int ch = 0; ch < kVChunks; ++ch)
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc)
+                        cp_async16(stage + (uint32_t)ch * kChunkBytes + 128u * (uint32_t)R + 16u * (uint32_t)(cc ^ (R & 7)),
+                                   g + (src ? ch * 128 + 16 * cc : 0), nb);
+            }
+            cp_async_commit();
+            if (it > 0) {
+                cp_async_wait<1>();
+                hand_over(it - 1);
+            }
+        }
+    }
+    cp_async_wait<0>();
+    if (ok && it > 0) hand_over(it - 1);
+    __syncwarp();
+}
+
 // Value-CTA TMA producer (one lane): whole pages (dims 0..511) through the V
 // ring (e4m3 cache: the page's 32 KB of codes into the upper half of the stage,
 // completing on B_VLAND; the row warps widen them and arrive on B_VFULL).
@@ -669,7 +839,7 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
             const int sb = step % kSBufs;
             const int scs = (int)(step % kScSlots);  // e4m3: this step's slot in the scale ring
             if (q2 == 0 && !warp_wait(c, B_SFULL + sb, (step / kSBufs) & 1)) return;
-            if (kFp8 && q2 == 0 && !warp_wait(c, B_SCFULL + scs, (step / kScSlots) & 1)) return;
+            if (kRing && q2 == 0 && !warp_wait(c, B_SCFULL + scs, (step / kScSlots) & 1)) return;
             tc_fence_after();
             uint32_t sr[64];
             {
@@ -681,6 +851,13 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
             // keys of this page visible to this row
             int nvalid = row_ok ? T_row - pg * kPage : 0;
             nvalid = nvalid < 0 ? 0 : (nvalid > kPage ? kPage : nvalid);
+            // sparse decode: the page's valid list entries (gathered rows)
+            uint64_t vmask = ~0ull;
+            if constexpr (kSparse) {
+                const uint32_t ms = smem_u32(c.base + kScaleOff) + (uint32_t)scs * kScBytes + (uint32_t)q2 * 8;
+                vmask = (uint64_t)lds32(ms) | ((uint64_t)lds32(ms + 4) << 32);
+                if (nvalid < kPage) vmask &= nvalid > 0 ? (~0ull >> (kPage - nvalid)) : 0ull;
+            }
             // e4m3 cache: the page's per-token scales (those of keys past the
             // visible ones, whatever the page holds there, read as 0)
             float cs[kFp8 ? kPage : 1];
@@ -703,7 +880,7 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
             if (q2 == 1 || pg == s.p1 - 1) {         // last page of the step: release its S buffer
                 tc_fence_before();
                 mbar_arrive(c.bar(B_SEMPTY + sb));
-                if constexpr (kFp8) mbar_arrive(c.bar(B_SCEMPTY + scs));  // the scales are in registers
+                if constexpr (kRing) mbar_arrive(c.bar(B_SCEMPTY + scs));  // the scales / masks are in registers
                 ++step;
             }
             if constexpr (kFp8) {
@@ -726,13 +903,15 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
             // (scaling is monotone there) and folds the scale into one FMA per
             // exponent below; otherwise the scaled, masked scores (-inf past
             // the visible keys) replace the raw ones and the FMA scale is 1.
-            const bool raw = nvalid == kPage && sc > 0.f;
+            const bool raw = nvalid == kPage && sc > 0.f && (!kSparse || vmask == ~0ull);
             const float fsc = raw ? sc : 1.f;
             float mx4[4] = {-CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F, -CUDART_INF_F};
             if (!raw) {
 #pragma unroll
-                for (int j = 0; j < 64; ++j)
-                    sr[j] = __float_as_uint((j < nvalid) ? __uint_as_float(sr[j]) * sc : -CUDART_INF_F);
+                for (int j = 0; j < 64; ++j) {
+                    const bool vis = kSparse ? ((vmask >> j) & 1ull) != 0 : j < nvalid;
+                    sr[j] = __float_as_uint(vis ? __uint_as_float(sr[j]) * sc : -CUDART_INF_F);
+                }
             }
 #pragma unroll
             for (int j = 0; j < 32; ++j)
@@ -1007,6 +1186,12 @@ split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParam
             mbar_init(c.bar(B_VFULL + i), kFp8 ? 128 : 1);  // e4m3: the 128 row threads that widened the page
             mbar_init(c.bar(B_VEMPTY + i), 1);
         }
+        if constexpr (kSparse) {
+            for (int i = 0; i < kScSlots; ++i) {
+                mbar_init(c.bar(B_SCFULL + i), 1);
+                mbar_init(c.bar(B_SCEMPTY + i), 128);
+            }
+        }
         if constexpr (kFp8) {
             for (int i = 0; i < kScoreIssuers * kLandSlots; ++i) mbar_init(c.bar(B_KLAND + i), 1);
             for (int i = 0; i < kVStages; ++i) mbar_init(c.bar(B_VLAND + i), 1);
@@ -1056,6 +1241,10 @@ split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParam
     if (warp == 0 || warp == 7) {
         if (kFp8 && is_score) {
             score_producer_e4m3(p, c, &kv_map, part, tile, warp == 0 ? 0 : 1);
+        } else if (kSparse && is_score) {
+            score_producer_sparse(p, c, part, tile, warp == 0 ? 0 : 1);
+        } else if (kSparse) {
+            if (warp == 0) value_producer_sparse(p, c, part, tile);
         } else if (elect_one_lane() && (warp == 0 || (is_score && kScoreIssuers > 1))) {
             if (is_score) score_producer(p, c, &kv_map, part, tile, warp == 0 ? 0 : 1);
             else value_producer(p, c, &kv_map, part);
@@ -1141,6 +1330,7 @@ cudaError_t prepare(int dev) {
 
 }  // namespace
 
+#if !MLA_SPLIT_SPARSE
 template <>
 cudaError_t split_kv_tc_max_pairs<kD, kFp8>(int *pairs) {
     int dev = 0;
@@ -1171,8 +1361,14 @@ cudaError_t split_kv_tc_max_pairs<kD, kFp8>(int *pairs) {
     return cudaSuccess;
 }
 
+#endif
+
+#if MLA_SPLIT_SPARSE
+cudaError_t launch_split_kv_tc_sparse(const DecodeParams &p, cudaStream_t stream) {
+#else
 template <>
 cudaError_t launch_split_kv_tc<kD, kFp8>(const DecodeParams &p, cudaStream_t stream) {
+#endif
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

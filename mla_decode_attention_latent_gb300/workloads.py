@@ -174,6 +174,22 @@ def pack_e4m3_pages(rows: torch.Tensor, scales: Optional[torch.Tensor] = None) -
     return out
 
 
+def make_index_lists(seqlens: Sequence[int], s_q: int, topk: int, seed: int):
+    """Seeded top-k style index lists for the sparse decode: int32 [b, s_q, topk].
+
+    Query token i of sequence b gets min(topk, T_b) distinct positions of
+    [0, T_b) in random order (a random permutation's prefix), the rest -1."""
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(seed)
+    out = torch.full((len(seqlens), s_q, topk), -1, dtype=torch.int32)
+    for b, T in enumerate(seqlens):
+        for i in range(s_q):
+            n = min(topk, int(T))
+            if n > 0:
+                out[b, i, :n] = torch.randperm(int(T), generator=gen)[:n].to(torch.int32)
+    return out
+
+
 def e4m3_page_codes(pages: torch.Tensor, d: int = D_QK, page: int = PAGE):
     """Views of packed pages: (codes uint8 [n, page, d], scales fp32 [n, page])."""
     n = pages.shape[0]

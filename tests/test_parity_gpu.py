@@ -325,3 +325,65 @@ def test_large_q_len(batch, s_q, h_q, seqlens):
     # many query tokens per step, causal: each row sees T - s_q + i + 1 keys,
     # and a 128-row tile holds 128 / h_q query tokens with different windows
     check(case(f"q{s_q}", batch, s_q, h_q, seqlens, causal=True, seed=140 + s_q))
+
+
+
+# ---------------------------------------------------------------- sparse top-k decode
+def sparse_check(batch, s_q, h_q, seqlens, topk, seed, num_parts=None, edit_lists=None):
+    import mla_decode_attention_latent_gb300 as mla
+    c = case("sparse", batch, s_q, h_q, seqlens, seed=seed)
+    x = W.make_inputs(c, "cpu")
+    idx = W.make_index_lists(seqlens, s_q, topk, seed)
+    if edit_lists is not None:
+        edit_lists(idx)
+    o_ref, lse_ref = oracle.mla_decode_sparse(W.bf16_bits(x.q), W.bf16_bits(x.kcache), x.block_table.numpy(),
+                                              x.cache_seqlens.numpy(), idx.numpy(), c.dv, c.softmax_scale)
+    xd = to_device(x, DEV)
+    lens = torch.full((batch,), topk, dtype=torch.int32, device=DEV)
+    md, ns = mla.mla_get_metadata(lens, c.num_q_rows, 1, num_parts=num_parts)
+    o, lse = mla.mla_decode_kvcache_sparse(xd.q, xd.kcache, xd.block_table, xd.cache_seqlens, idx.to(DEV), c.dv,
+                                           md, ns, list_lens=lens, softmax_scale=c.softmax_scale)
+    torch.cuda.synchronize()
+    st = mla.mla_device_status(clear=True)
+    assert st == 0, f"device status {st:#x}"
+    assert_parity(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, f"sparse b={batch} s_q={s_q} topk={topk}")
+    return o, lse
+
+
+@pytest.mark.parametrize("batch,s_q,h_q,seqlens,topk,parts", [
+    (2, 1, 16, [300, 37], 64, None),                  # the second list is padded with -1
+    (3, 1, 128, [1000, 77, 2100], 256, 1),            # one part walks every sequence's lists
+    (3, 1, 128, [1000, 77, 2100], 256, 3),            # lists cut between parts
+    (3, 1, 128, [1000, 77, 2100], 256, None),
+    (2, 2, 128, [700, 130], 100, None),               # two query tokens (two tiles), a partial last chunk
+    (2, 1, 128, [4096, 0], 2048, None),               # a long list, and a sequence with an empty cache
+])
+def test_sparse_decode(batch, s_q, h_q, seqlens, topk, parts):
+    sparse_check(batch, s_q, h_q, seqlens, topk, seed=150 + topk + batch, num_parts=parts)
+
+
+def test_sparse_decode_junk_entries():
+    # repeated positions count twice; -1, negative and past-the-end entries are ignored
+    def edit(idx):
+        idx[0, 0, 1] = idx[0, 0, 0]
+        idx[0, 0, 2] = 300
+        idx[0, 0, 3] = -7
+        idx[1, 0, 5] = 10 ** 6
+        idx[1, 0, 6] = idx[1, 0, 7]
+    sparse_check(2, 1, 32, [300, 200], 130, seed=160, edit_lists=edit)
+
+
+def test_sparse_full_list_matches_dense():
+    # the list 0 .. T-1 is the dense decode
+    import mla_decode_attention_latent_gb300 as mla
+    seqlens = [500, 130]
+    c = case("sparse-full", 2, 1, 128, seqlens, seed=161)
+    x = to_device(W.make_inputs(c, "cpu"), DEV)
+    idx = torch.full((2, 1, 512), -1, dtype=torch.int32)
+    for b, T in enumerate(seqlens):
+        idx[b, 0, :T] = torch.arange(T, dtype=torch.int32)
+    o_s, l_s = mla.mla_decode_kvcache_sparse(x.q, x.kcache, x.block_table, x.cache_seqlens, idx.to(DEV), c.dv,
+                                             softmax_scale=c.softmax_scale)
+    o_d, l_d, *_ = run_gpu(x)
+    assert mla.mla_device_status(clear=True) == 0
+    assert torch.allclose(o_s.float(), o_d.float(), rtol=1e-2, atol=2e-3) and torch.allclose(l_s, l_d, atol=1e-4)
