@@ -142,3 +142,35 @@ def test_fp8_page_bytes():
     text = open(HEADER).read()
     assert "#define MLA_FP8_PAGE_BYTES(d) (MLA_PAGE_SIZE * (d) + MLA_PAGE_SIZE * 4)" in text
     assert _lib.MLA_FP8_PAGE_BYTES(576) == 37120
+
+
+def _decode_sparse(lib, **over):
+    a = dict(q=16, kc=16, num_blocks=4, bt=16, max_blocks=2, sl=16, idx=16, topk=64, lens=16, batch=2, s_q=1, h_q=16,
+             h_kv=1, d=576, dv=512, md=16, ns=16, num_parts=3, scale=1 / 24, o=16, lse=16, ws=256, ws_bytes=1 << 30)
+    a.update(over)
+    return lib.mla_decode_kvcache_sparse(a["q"], a["kc"], a["num_blocks"], a["bt"], a["max_blocks"], a["sl"], a["idx"],
+                                         a["topk"], a["lens"], a["batch"], a["s_q"], a["h_q"], a["h_kv"], a["d"], a["dv"],
+                                         a["md"], a["ns"], a["num_parts"], a["scale"], a["o"], a["lse"], a["ws"],
+                                         a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(idx=None), _lib.MLA_ERR_INVALID_ARG),
+    (dict(lens=None), _lib.MLA_ERR_INVALID_ARG),
+    (dict(topk=0), _lib.MLA_ERR_INVALID_ARG),
+    (dict(d=512), _lib.MLA_ERR_UNSUPPORTED),           # 576-wide rows only
+    (dict(s_q=2, h_q=64), _lib.MLA_ERR_UNSUPPORTED),   # a row tile must hold one query token
+    (dict(ws_bytes=1024), _lib.MLA_ERR_WORKSPACE),
+])
+def test_sparse_decode_rejects_bad_arguments_before_launch(lib, over, code):
+    assert _decode_sparse(lib, **over) == code
+
+
+def test_index_lists_generator():
+    from mla_decode_attention_latent_gb300 import workloads as W
+    idx = W.make_index_lists([100, 3, 0], 2, 8, seed=1)
+    assert idx.shape == (3, 2, 8) and idx.dtype.is_floating_point is False
+    for i in range(2):
+        assert sorted(idx[0, i].tolist()) == sorted(set(idx[0, i].tolist())) and min(idx[0, i].tolist()) >= 0
+        assert sorted(idx[1, i, :3].tolist()) == [0, 1, 2] and idx[1, i, 3:].tolist() == [-1] * 5
+        assert idx[2, i].tolist() == [-1] * 8
