@@ -190,8 +190,8 @@ int mla_decode_kvcache(const void *q, const void *kcache, int64_t num_blocks, co
                        int h_kv, int d, int dv, const int32_t *tile_scheduler_metadata,
                        const int32_t *num_splits, int num_parts, float softmax_scale, int causal, void *o,
                        float *lse, void *workspace, size_t ws_bytes, struct CUstream_st *stream) {
-    return decode(q, kcache, Kind::kBf16, num_blocks, block_table, max_blocks_per_seq, cache_seqlens, batch, s_q, h_q, h_kv,
-                  d, dv, tile_scheduler_metadata, num_splits, num_parts, softmax_scale, causal, o, lse, workspace,
+    return decode(q, kcache, Kind::kBf16, num_blocks, block_table, max_blocks_per_seq, cache_seqlens, batch, s_q, h_q,
+                  h_kv, d, dv, tile_scheduler_metadata, num_splits, num_parts, softmax_scale, causal, o, lse, workspace,
                   ws_bytes, stream);
 }
 
@@ -200,8 +200,8 @@ int mla_decode_kvcache_fp8(const void *q, const void *kv_pages, int64_t num_bloc
                            int h_kv, int d, int dv, const int32_t *tile_scheduler_metadata,
                            const int32_t *num_splits, int num_parts, float softmax_scale, int causal, void *o,
                            float *lse, void *workspace, size_t ws_bytes, struct CUstream_st *stream) {
-    return decode(q, kv_pages, Kind::kE4m3, num_blocks, block_table, max_blocks_per_seq, cache_seqlens, batch, s_q, h_q, h_kv,
-                  d, dv, tile_scheduler_metadata, num_splits, num_parts, softmax_scale, causal, o, lse, workspace,
+    return decode(q, kv_pages, Kind::kE4m3, num_blocks, block_table, max_blocks_per_seq, cache_seqlens, batch, s_q,
+                  h_q, h_kv, d, dv, tile_scheduler_metadata, num_splits, num_parts, softmax_scale, causal, o, lse, workspace,
                   ws_bytes, stream);
 }
 

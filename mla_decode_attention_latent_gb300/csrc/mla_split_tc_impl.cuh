@@ -533,9 +533,12 @@ __device__ void score_producer_sparse(const DecodeParams &p, const Ctx &c, int p
             const uint8_t *src[4];
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4)
-                src[q4] = (q4 < 2 || npg > 1) ? sparse_row(p, list, list_len, T, s.b, kPage * pg + 32 * q4 + lane) : nullptr;
-            const uint32_t m0 = __ballot_sync(0xffffffffu, src[0] != nullptr), m1 = __ballot_sync(0xffffffffu, src[1] != nullptr),
-                           m2 = __ballot_sync(0xffffffffu, src[2] != nullptr), m3 = __ballot_sync(0xffffffffu, src[3] != nullptr);
+                src[q4] = (q4 < 2 || npg > 1) ? sparse_row(p, list, list_len, T, s.b, kPage * pg + 32 * q4 + lane)
+                                              : nullptr;
+            const uint32_t m0 = __ballot_sync(0xffffffffu, src[0] != nullptr),
+                           m1 = __ballot_sync(0xffffffffu, src[1] != nullptr),
+                           m2 = __ballot_sync(0xffffffffu, src[2] != nullptr),
+                           m3 = __ballot_sync(0xffffffffu, src[3] != nullptr);
             const int sc = (int)(step % kScSlots);
             if (!warp_wait(c, B_SCEMPTY + sc, ((step / kScSlots) & 1) ^ 1)) {
                 ok = false;
@@ -561,7 +564,8 @@ __device__ void score_producer_sparse(const DecodeParams &p, const Ctx &c, int p
                     const uint8_t *g = src[q4] ? src[q4] + ch * 128 : reinterpret_cast<const uint8_t *>(p.kcache);
                     const uint32_t nb = src[q4] ? 16u : 0u;
 #pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) cp_async16(row + 16u * (uint32_t)(cc ^ (R & 7)), g + (src[q4] ? 16 * cc : 0), nb);
+                    for (int cc = 0; cc < 8; ++cc)
+                        cp_async16(row + 16u * (uint32_t)(cc ^ (R & 7)), g + (src[q4] ? 16 * cc : 0), nb);
                 }
                 cp_async_commit();
                 ++issued;
@@ -616,7 +620,8 @@ __device__ void value_producer_sparse(const DecodeParams &p, const Ctx &c, int p
                 for (int ch = 0; ch < kVChunks; ++ch)
 #pragma unroll
                     for (int cc = 0; cc < 8; ++cc)
-                        cp_async16(stage + (uint32_t)ch * kChunkBytes + 128u * (uint32_t)R + 16u * (uint32_t)(cc ^ (R & 7)),
+                        cp_async16(stage + (uint32_t)ch * kChunkBytes + 128u * (uint32_t)R +
+                                       16u * (uint32_t)(cc ^ (R & 7)),
                                    g + (src ? ch * 128 + 16 * cc : 0), nb);
             }
             cp_async_commit();
@@ -862,7 +867,8 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
             // visible ones, whatever the page holds there, read as 0)
             float cs[kFp8 ? kPage : 1];
             if constexpr (kFp8) {
-                const uint32_t sc_s = smem_u32(c.base + kScaleOff) + (uint32_t)scs * kScBytes + (uint32_t)q2 * kPage * 4;
+                const uint32_t sc_s =
+                    smem_u32(c.base + kScaleOff) + (uint32_t)scs * kScBytes + (uint32_t)q2 * kPage * 4;
 #pragma unroll
                 for (int j = 0; j < kPage / 4; ++j) {
                     const uint4 c4 = lds128(sc_s + 16 * j);
