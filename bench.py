@@ -52,7 +52,7 @@ METRIC = "MLA decode µs/call, KV-cache GB/s and TFLOPS vs GB300 roofline"
 def workload_label(case):
     """The workload named by what it is, with its sizes (the same string in both arms)."""
     lengths = "U" + str(case.seqlen_range) if case.seqlen_range else case.seqlens[0]
-    cache = ", cache=e4m3+per-token fp32 scales" if case.fp8 else ""
+    cache = ", cache=e4m3+per-token fp32 scales" if case.fp8 else (f", sparse topk={case.topk}" if case.topk else "")
     return (f"{case.name}: b={case.batch}, s_q={case.s_q}, h_q={case.h_q}, h_kv={case.h_kv}, d={case.d}, "
             f"dv={case.dv}, page={case.page}, causal={case.causal}, seqlens={lengths}{cache}")
 
@@ -61,6 +61,16 @@ def workload_figures(case, seqlens):
     """Algorithmic bytes and FLOPs of one decode call."""
     from mla_decode_attention_latent_gb300 import workloads as W
     page_bytes = case.page_bytes  # bf16 rows, or e4m3 codes + fp32 scales
+    if case.topk:
+        # sparse: the gathered rows and the index lists are the cache-side bytes
+        entries = W.valid_list_entries(case, seqlens)
+        kv_bytes = entries * case.h_kv * case.d * 2 + case.batch * case.s_q * case.topk * 4
+        q_bytes = case.batch * case.s_q * case.h_q * case.d * 2
+        o_bytes = case.batch * case.s_q * case.h_q * case.dv * 2
+        lse_bytes = case.batch * case.s_q * case.h_q * 4
+        flops = 2.0 * case.h_q * (case.d + case.dv) * entries
+        return {"bytes": kv_bytes + q_bytes + o_bytes + lse_bytes, "kv_bytes": kv_bytes, "flops": flops,
+                "valid_token_bytes": entries * case.h_kv * case.d * 2}
     kv_bytes = W.kv_pages_touched(seqlens, case.page) * page_bytes
     q_bytes = case.batch * case.s_q * case.h_q * case.d * 2
     o_bytes = case.batch * case.s_q * case.h_q * case.dv * 2
@@ -262,8 +272,14 @@ def time_oracle(case, x_cpu, budget_s=10.0, max_seqs=None):
     sl = x_cpu.cache_seqlens.numpy()
     q_bits = W.bf16_bits(x_cpu.q)
     k_data = x_cpu.kcache.numpy() if case.fp8 else W.bf16_bits(x_cpu.kcache)
-    decode = oracle.mla_decode_fp8 if case.fp8 else oracle.mla_decode
     bt = x_cpu.block_table.numpy()
+    if case.topk:
+        idx = x_cpu.indices.numpy()
+
+        def decode(q, k, bt_, sl_, dv, scale, causal, rows):
+            return oracle.mla_decode_sparse(q, k, bt_, sl_, idx, dv, scale, rows=rows)
+    else:
+        decode = oracle.mla_decode_fp8 if case.fp8 else oracle.mla_decode
 
     def run(seqs):
         rows = np.concatenate([np.arange(b * R, (b + 1) * R, dtype=np.int64) for b in seqs])
@@ -275,7 +291,8 @@ def time_oracle(case, x_cpu, budget_s=10.0, max_seqs=None):
     n = max(1, min(case.batch if max_seqs is None else max_seqs, int(budget_s / max(t1, 1e-6))))
     seqs = list(range(n))
     t = run(seqs)
-    frac_keys = sum(int(sl[b]) for b in seqs) / max(1, sum(int(s) for s in sl))
+    work = [min(case.topk, int(s)) if case.topk else int(s) for s in sl]  # keys each sequence's rows see
+    frac_keys = sum(work[b] for b in seqs) / max(1, sum(work))
     return {"seconds": t, "seqs": n, "call_seconds": t / frac_keys, "cores": oracle.max_threads()}
 
 
@@ -311,7 +328,10 @@ def main():
     fig = workload_figures(case, sl_list)
     stream = torch.cuda.current_stream(dev)
 
-    md, ns = mla.mla_get_metadata(x.cache_seqlens, case.num_q_rows, case.h_kv)
+    # the work partition runs on the cache lengths, or on the list lengths (sparse)
+    part_lens = (torch.full((case.batch,), case.topk, dtype=torch.int32, device=dev) if case.topk
+                 else x.cache_seqlens)
+    md, ns = mla.mla_get_metadata(part_lens, case.num_q_rows, case.h_kv)
     num_parts = md.shape[0]
     o = torch.empty((case.batch, case.s_q, case.h_q, case.dv), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((case.batch, case.s_q, case.h_q), dtype=torch.float32, device=dev)
@@ -321,9 +341,14 @@ def main():
     decode = mla.mla_decode_kvcache_fp8 if case.fp8 else mla.mla_decode_kvcache
 
     def step():
-        md_k, ns_k = mla.mla_get_metadata(x.cache_seqlens, case.num_q_rows, case.h_kv, num_parts=num_parts)
-        decode(x.q, x.kcache, x.block_table, x.cache_seqlens, case.dv, md_k, ns_k, softmax_scale=case.softmax_scale,
-               causal=case.causal, out=o, lse=lse, workspace=ws)
+        md_k, ns_k = mla.mla_get_metadata(part_lens, case.num_q_rows, case.h_kv, num_parts=num_parts)
+        if case.topk:
+            mla.mla_decode_kvcache_sparse(x.q, x.kcache, x.block_table, x.cache_seqlens, x.indices, case.dv, md_k,
+                                          ns_k, list_lens=part_lens, softmax_scale=case.softmax_scale, out=o, lse=lse,
+                                          workspace=ws)
+        else:
+            decode(x.q, x.kcache, x.block_table, x.cache_seqlens, case.dv, md_k, ns_k,
+                   softmax_scale=case.softmax_scale, causal=case.causal, out=o, lse=lse, workspace=ws)
 
     for _ in range(args.warmup):
         step()
@@ -383,7 +408,8 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         x_cpu = W.make_inputs(case, device="cpu") if case.name == "tiny" else \
-            W.Inputs(case, x.q.cpu(), x.kcache.cpu(), x.block_table.cpu(), x.cache_seqlens.cpu())
+            W.Inputs(case, x.q.cpu(), x.kcache.cpu(), x.block_table.cpu(), x.cache_seqlens.cpu(),
+                     None if x.indices is None else x.indices.cpu())
         t = time_oracle(case, x_cpu)
         cpu = {"value": fig["bytes"] / t["call_seconds"] / 1e9, "unit": "GB/s", "cores": t["cores"],
                "kind": "oracle", "us_per_call": t["call_seconds"] * 1e6,
@@ -430,14 +456,24 @@ def e2e_run(mla, case, x, fig, dev, stream, steps, world):
     dq, dk = torch.empty_like(x.q), torch.empty_like(x.kcache)
     dbt, dsl = torch.empty_like(x.block_table), torch.empty_like(x.cache_seqlens)
     decode = mla.mla_decode_kvcache_fp8 if case.fp8 else mla.mla_decode_kvcache
+    if case.topk:
+        hidx = x.indices.cpu().pin_memory()
+        didx = torch.empty_like(x.indices)
+        lens = torch.full((case.batch,), case.topk, dtype=torch.int32, device=dev)
 
     def one():
         dq.copy_(hq, non_blocking=True)
         dk.copy_(hk, non_blocking=True)
         dbt.copy_(hbt, non_blocking=True)
         dsl.copy_(hsl, non_blocking=True)
-        md, ns = mla.mla_get_metadata(dsl, case.num_q_rows, case.h_kv)
-        o, lse = decode(dq, dk, dbt, dsl, case.dv, md, ns, softmax_scale=case.softmax_scale, causal=case.causal)
+        if case.topk:
+            didx.copy_(hidx, non_blocking=True)
+            md, ns = mla.mla_get_metadata(lens, case.num_q_rows, case.h_kv)
+            o, lse = mla.mla_decode_kvcache_sparse(dq, dk, dbt, dsl, didx, case.dv, md, ns, list_lens=lens,
+                                                   softmax_scale=case.softmax_scale)
+        else:
+            md, ns = mla.mla_get_metadata(dsl, case.num_q_rows, case.h_kv)
+            o, lse = decode(dq, dk, dbt, dsl, case.dv, md, ns, softmax_scale=case.softmax_scale, causal=case.causal)
         ho.copy_(o, non_blocking=True)
         hl.copy_(lse, non_blocking=True)
 
@@ -452,7 +488,7 @@ def e2e_run(mla, case, x, fig, dev, stream, steps, world):
     b.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(a.elapsed_time(b) / steps, world)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hbt, hsl))
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hbt, hsl) + ((hidx,) if case.topk else ()))
     d2h = sum(t.numel() * t.element_size() for t in (ho, hl))
     return {"value": round(fig["bytes"] * world / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}

@@ -59,6 +59,7 @@ class Case:
     pool_pages: Optional[int] = None             # physical pages; default = pages needed
     seed: int = 0
     fp8: bool = False                            # packed e4m3 pages with per-token scales
+    topk: int = 0                                # > 0: sparse decode over index lists of this length
 
     @property
     def page_bytes(self) -> int:
@@ -84,7 +85,10 @@ LONG = Case("long", batch=64, s_q=1, h_q=128, seqlens=(65536,) * 64, seed=4)
 UNIFORM_D512 = Case("uniform_d512", batch=64, s_q=1, h_q=128, seqlens=(4096,) * 64, pool_pages=4096, seed=5, d=512)
 # the uniform decode over an e4m3 cache with per-token scales
 UNIFORM_FP8 = Case("uniform_fp8", batch=64, s_q=1, h_q=128, seqlens=(4096,) * 64, pool_pages=4096, seed=6, fp8=True)
-CASES = {c.name: c for c in (TINY, UNIFORM, VARIABLE, MTP, LONG, UNIFORM_D512, UNIFORM_FP8)}
+# sparse top-k decode: 2048 listed tokens per query over 32768-token caches
+SPARSE = Case("sparse", batch=64, s_q=1, h_q=128, seqlens=(32768,) * 64, seed=7, topk=2048)
+TINY_SPARSE = Case("tiny_sparse", batch=2, s_q=1, h_q=16, seqlens=(300, 37), pool_pages=8, seed=8, topk=64)
+CASES = {c.name: c for c in (TINY, UNIFORM, VARIABLE, MTP, LONG, UNIFORM_D512, UNIFORM_FP8, SPARSE, TINY_SPARSE)}
 
 
 @dataclasses.dataclass
@@ -94,6 +98,7 @@ class Inputs:
     kcache: torch.Tensor         # [num_blocks, page, h_kv, d] bf16, or uint8 [num_blocks, page_bytes] (fp8)
     block_table: torch.Tensor    # [b, max_blocks] int32
     cache_seqlens: torch.Tensor  # [b] int32
+    indices: Optional[torch.Tensor] = None  # [b, s_q, topk] int32 (sparse cases)
 
 
 def draw_seqlens(case: Case, gen: torch.Generator) -> torch.Tensor:
@@ -155,7 +160,16 @@ def make_inputs(case: Case, device: str = "cpu", seqlens: Optional[Sequence[int]
             kcache[s:e] = pack_e4m3_pages(x[:, :, 0, :])
         else:
             kcache[s:e] = x.to(torch.bfloat16)
-    return Inputs(case, q, kcache, bt.to(device), sl.to(device))
+    indices = None
+    if case.topk > 0:
+        indices = make_index_lists(sl.tolist(), case.s_q, case.topk, case.seed + 17).to(device)
+    return Inputs(case, q, kcache, bt.to(device), sl.to(device), indices)
+
+
+def valid_list_entries(case: Case, seqlens: Sequence[int]) -> int:
+    """Valid entries over all index lists of a sparse case (``make_index_lists``
+    lists hold min(topk, T_b) distinct positions per query token)."""
+    return sum(case.s_q * min(case.topk, int(t)) for t in seqlens)
 
 
 def pack_e4m3_pages(rows: torch.Tensor, scales: Optional[torch.Tensor] = None) -> torch.Tensor:

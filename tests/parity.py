@@ -65,7 +65,8 @@ def oracle_of(x: W.Inputs, rows=None):
 
 
 def to_device(x: W.Inputs, dev) -> W.Inputs:
-    return W.Inputs(x.case, x.q.to(dev), x.kcache.to(dev), x.block_table.to(dev), x.cache_seqlens.to(dev))
+    return W.Inputs(x.case, x.q.to(dev), x.kcache.to(dev), x.block_table.to(dev), x.cache_seqlens.to(dev),
+                    None if x.indices is None else x.indices.to(dev))
 
 
 def run_gpu(x: W.Inputs, num_parts=None):

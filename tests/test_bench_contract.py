@@ -60,6 +60,25 @@ def test_fp8_figures_count_packed_pages():
     assert "e4m3" in bench.workload_label(W.UNIFORM_FP8)
 
 
+def test_sparse_figures_count_gathered_rows():
+    # 64 sequences x 2048 valid entries x 1152 B of gathered rows + the int32 lists
+    fig = bench.workload_figures(W.SPARSE, seqlens_of(W.SPARSE))
+    assert fig["kv_bytes"] == 64 * 2048 * 1152 + 64 * 2048 * 4
+    assert fig["flops"] == 2.0 * 128 * 1088 * 64 * 2048
+    tiny = bench.workload_figures(W.TINY_SPARSE, seqlens_of(W.TINY_SPARSE))
+    assert tiny["kv_bytes"] == (64 + 37) * 1152 + 2 * 64 * 4      # the 37-token cache lists 37 entries
+
+
+def test_sparse_reference_arm_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                          "tiny_sparse", "--steps", "1", "--warmup", "3"], capture_output=True, text=True, timeout=300,
+                         cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert "sparse topk=64" in line["config"]["workload"]
+
+
 def test_workload_label_names_the_sizes():
     label = bench.workload_label(W.UNIFORM_D512)
     assert label.startswith("uniform_d512: b=64, s_q=1, h_q=128") and "d=512" in label
