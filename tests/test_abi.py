@@ -174,3 +174,11 @@ def test_index_lists_generator():
         assert sorted(idx[0, i].tolist()) == sorted(set(idx[0, i].tolist())) and min(idx[0, i].tolist()) >= 0
         assert sorted(idx[1, i, :3].tolist()) == [0, 1, 2] and idx[1, i, 3:].tolist() == [-1] * 5
         assert idx[2, i].tolist() == [-1] * 8
+
+
+def test_valid_list_entries_counts_the_generated_lists():
+    from mla_decode_attention_latent_gb300 import workloads as W
+    c = W.TINY_SPARSE
+    x = W.make_inputs(c)
+    counted = int(((x.indices >= 0) & (x.indices < x.cache_seqlens[:, None, None])).sum())
+    assert counted == W.valid_list_entries(c, x.cache_seqlens.tolist())
