@@ -182,3 +182,18 @@ def test_valid_list_entries_counts_the_generated_lists():
     x = W.make_inputs(c)
     counted = int(((x.indices >= 0) & (x.indices < x.cache_seqlens[:, None, None])).sum())
     assert counted == W.valid_list_entries(c, x.cache_seqlens.tolist())
+
+
+def test_header_is_a_c_abi(lib, tmp_path):
+    # a plain C11 program includes the header, links the library and calls it
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    here = os.path.dirname(os.path.abspath(__file__))
+    so = _lib.LIB_PATH
+    exe = str(tmp_path / "abi_from_c")
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), os.path.join(here, "abi_from_c.c"),
+                    so, "-Wl,-rpath," + os.path.dirname(so), "-o", exe], check=True)
+    out = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0 and out.stdout.strip() == "ok", out.stderr
