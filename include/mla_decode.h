@@ -35,6 +35,11 @@
  *    nothing is launched and no output is touched.
  *  - bf16 tensors are raw IEEE bfloat16 bit patterns (2 bytes per element),
  *    row-major and densely packed in the shapes given.
+ *  - The library looks up the device addresses of its own device arrays (the
+ *    status word, the scratch of mla_decode_kvcache_noalloc) once per device
+ *    and keeps them for the life of the process.  cudaDeviceReset invalidates
+ *    them: do not call the library on a device after resetting it in the same
+ *    process.
  *
  * Supported on the GPU path: d = 576 or 512 (bf16 cache) or 576 (packed
  * e4m3 cache, mla_decode_kvcache_fp8), dv = 512, page size 64,

@@ -71,12 +71,12 @@ def mla_workspace_bytes(batch: int, s_q: int, h_q: int, h_kv: int, dv: int, num_
     return int(n)
 
 
-def mla_decode_kvcache(q: torch.Tensor, kcache: torch.Tensor, block_table: torch.Tensor,
-                       cache_seqlens: torch.Tensor, dv: int, tile_scheduler_metadata: torch.Tensor,
-                       num_splits: torch.Tensor, softmax_scale: Optional[float] = None, causal: bool = False,
-                       out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-                       workspace: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """MLA decode: returns (o bf16 [b, s_q, h_q, dv], lse fp32 [b, s_q, h_q])."""
+def _dense_decode_args(q, kcache, block_table, cache_seqlens, dv, tile_scheduler_metadata, num_splits, out, lse,
+                       allocate):
+    """Check the tensors of a decode over a bf16 cache; return (b, s_q, h_q, d, num_blocks, h_kv, num_parts, out,
+    lse).  Shapes are checked here, before the library is called, so that a
+    wrongly shaped tensor can never make a kernel read or write out of bounds;
+    ``allocate`` creates missing outputs (otherwise they are required)."""
     _need_cuda("q", q, torch.bfloat16)
     _need_cuda("kcache", kcache, torch.bfloat16)
     _need_cuda("block_table", block_table, torch.int32)
@@ -93,22 +93,42 @@ def mla_decode_kvcache(q: torch.Tensor, kcache: torch.Tensor, block_table: torch
         raise ValueError("batch size differs between q, block_table, cache_seqlens and num_splits")
     if tile_scheduler_metadata.dim() != 2 or tile_scheduler_metadata.shape[1] != MLA_METADATA_INTS:
         raise ValueError("tile_scheduler_metadata must be [num_parts, 8]")
-    num_parts = tile_scheduler_metadata.shape[0]
     dev = q.device
-    if softmax_scale is None:
-        softmax_scale = 1.0 / math.sqrt(d)
-    if out is None:
+    if out is None and allocate:
         out = torch.empty((b, s_q, h_q, dv), dtype=torch.bfloat16, device=dev)
-    if lse is None:
+    if lse is None and allocate:
         lse = torch.empty((b, s_q, h_q), dtype=torch.float32, device=dev)
     _need_cuda("out", out, torch.bfloat16)
     _need_cuda("lse", lse, torch.float32)
     if tuple(out.shape) != (b, s_q, h_q, dv) or tuple(lse.shape) != (b, s_q, h_q):
         raise ValueError("out must be [b, s_q, h_q, dv] and lse [b, s_q, h_q]")
+    _same_device(dev, kcache=kcache, block_table=block_table, cache_seqlens=cache_seqlens,
+                 tile_scheduler_metadata=tile_scheduler_metadata, num_splits=num_splits, out=out, lse=lse)
+    return b, s_q, h_q, d, num_blocks, h_kv, tile_scheduler_metadata.shape[0], out, lse
+
+
+def _same_device(dev: torch.device, **tensors) -> None:
+    for name, t in tensors.items():
+        if t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, but q is on {dev}")
+
+
+def mla_decode_kvcache(q: torch.Tensor, kcache: torch.Tensor, block_table: torch.Tensor,
+                       cache_seqlens: torch.Tensor, dv: int, tile_scheduler_metadata: torch.Tensor,
+                       num_splits: torch.Tensor, softmax_scale: Optional[float] = None, causal: bool = False,
+                       out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """MLA decode: returns (o bf16 [b, s_q, h_q, dv], lse fp32 [b, s_q, h_q])."""
+    b, s_q, h_q, d, num_blocks, h_kv, num_parts, out, lse = _dense_decode_args(
+        q, kcache, block_table, cache_seqlens, dv, tile_scheduler_metadata, num_splits, out, lse, allocate=True)
+    dev = q.device
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(d)
     ws_need = mla_workspace_bytes(b, s_q, h_q, h_kv, dv, num_parts) if dv == MLA_V_DIM and h_q % h_kv == 0 else 256
     if workspace is None:
         workspace = torch.empty((ws_need,), dtype=torch.uint8, device=dev)
     _need_cuda("workspace", workspace, torch.uint8)
+    _same_device(dev, workspace=workspace)
     with torch.cuda.device(dev):
         st = load().mla_decode_kvcache(
             q.data_ptr(), kcache.data_ptr(), num_blocks, block_table.data_ptr(), block_table.shape[1],
@@ -163,6 +183,9 @@ def mla_decode_kvcache_fp8(q: torch.Tensor, kv_pages: torch.Tensor, block_table:
     if workspace is None:
         workspace = torch.empty((ws_need,), dtype=torch.uint8, device=dev)
     _need_cuda("workspace", workspace, torch.uint8)
+    _same_device(dev, kv_pages=kv_pages, block_table=block_table, cache_seqlens=cache_seqlens,
+                 tile_scheduler_metadata=tile_scheduler_metadata, num_splits=num_splits, out=out, lse=lse,
+                 workspace=workspace)
     with torch.cuda.device(dev):
         st = load().mla_decode_kvcache_fp8(
             q.data_ptr(), kv_pages.data_ptr(), num_blocks, block_table.data_ptr(), block_table.shape[1],
@@ -204,6 +227,11 @@ def mla_decode_kvcache_sparse(q: torch.Tensor, kcache: torch.Tensor, block_table
         tile_scheduler_metadata, num_splits = mla_get_metadata(list_lens, s_q * h_q // h_kv, h_kv)
     _need_cuda("tile_scheduler_metadata", tile_scheduler_metadata, torch.int32)
     _need_cuda("num_splits", num_splits, torch.int32)
+    if (block_table.dim() != 2 or block_table.shape[0] != b or cache_seqlens.numel() != b or list_lens.numel() != b
+            or num_splits.numel() != b + 1):
+        raise ValueError("batch size differs between q, block_table, cache_seqlens, list_lens and num_splits")
+    if tile_scheduler_metadata.dim() != 2 or tile_scheduler_metadata.shape[1] != MLA_METADATA_INTS:
+        raise ValueError("tile_scheduler_metadata must be [num_parts, 8]")
     num_parts = tile_scheduler_metadata.shape[0]
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(d)
@@ -213,10 +241,16 @@ def mla_decode_kvcache_sparse(q: torch.Tensor, kcache: torch.Tensor, block_table
         lse = torch.empty((b, s_q, h_q), dtype=torch.float32, device=dev)
     _need_cuda("out", out, torch.bfloat16)
     _need_cuda("lse", lse, torch.float32)
+    if tuple(out.shape) != (b, s_q, h_q, dv) or tuple(lse.shape) != (b, s_q, h_q):
+        raise ValueError("out must be [b, s_q, h_q, dv] and lse [b, s_q, h_q]")
+    _same_device(dev, kcache=kcache, block_table=block_table, cache_seqlens=cache_seqlens, indices=indices,
+                 list_lens=list_lens, tile_scheduler_metadata=tile_scheduler_metadata, num_splits=num_splits,
+                 out=out, lse=lse)
     ws_need = mla_workspace_bytes(b, s_q, h_q, h_kv, dv, num_parts) if dv == MLA_V_DIM and h_q % h_kv == 0 else 256
     if workspace is None:
         workspace = torch.empty((ws_need,), dtype=torch.uint8, device=dev)
     _need_cuda("workspace", workspace, torch.uint8)
+    _same_device(dev, workspace=workspace)
     with torch.cuda.device(dev):
         st = load().mla_decode_kvcache_sparse(
             q.data_ptr(), kcache.data_ptr(), num_blocks, block_table.data_ptr(), block_table.shape[1],
@@ -238,14 +272,8 @@ def mla_decode_kvcache_noalloc(q: torch.Tensor, kcache: torch.Tensor, block_tabl
     by every call, so calls must not overlap on the GPU.  Make the first call
     on a device before any stream capture (it looks up the array's address).
     """
-    for name, t, dt in (("q", q, torch.bfloat16), ("kcache", kcache, torch.bfloat16),
-                        ("block_table", block_table, torch.int32), ("cache_seqlens", cache_seqlens, torch.int32),
-                        ("tile_scheduler_metadata", tile_scheduler_metadata, torch.int32),
-                        ("num_splits", num_splits, torch.int32), ("out", out, torch.bfloat16),
-                        ("lse", lse, torch.float32)):
-        _need_cuda(name, t, dt)
-    b, s_q, h_q, d = q.shape
-    num_blocks, _, h_kv, _ = kcache.shape
+    b, s_q, h_q, d, num_blocks, h_kv, num_parts, out, lse = _dense_decode_args(
+        q, kcache, block_table, cache_seqlens, dv, tile_scheduler_metadata, num_splits, out, lse, allocate=False)
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(d)
     dev = q.device
@@ -253,7 +281,7 @@ def mla_decode_kvcache_noalloc(q: torch.Tensor, kcache: torch.Tensor, block_tabl
         st = load().mla_decode_kvcache_noalloc(
             q.data_ptr(), kcache.data_ptr(), num_blocks, block_table.data_ptr(), block_table.shape[1],
             cache_seqlens.data_ptr(), b, s_q, h_q, h_kv, d, dv, tile_scheduler_metadata.data_ptr(),
-            num_splits.data_ptr(), tile_scheduler_metadata.shape[0], float(softmax_scale), int(bool(causal)),
+            num_splits.data_ptr(), num_parts, float(softmax_scale), int(bool(causal)),
             out.data_ptr(), lse.data_ptr(), _stream_handle(dev))
     check("mla_decode_kvcache_noalloc", st)
 

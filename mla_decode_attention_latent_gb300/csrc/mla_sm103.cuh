@@ -151,17 +151,6 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
-// 3-D tiled load written to the same shared-memory offset of every CTA in
-// `cta_mask`; completes tx bytes on the barrier at `bar`'s offset in each.
-__device__ __forceinline__ void tma_load_3d_multicast(void *dst, const CUtensorMap *map, uint64_t *bar, int c0,
-                                                      int c1, int c2, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, "
-        "{%3, %4, %5}], [%2], %6;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "h"(cta_mask)
-        : "memory");
-}
-
 // bulk copy of `bytes` from this CTA's shared memory into a peer CTA's shared
 // memory; completes the transaction bytes on the peer's barrier
 __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const void *src, uint32_t bytes,
@@ -198,12 +187,12 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// prefetch a contiguous global range into L2
 // bring the line holding `src` into L1 (no register result, never faults)
 __device__ __forceinline__ void prefetch_line_l1(const void *src) {
     asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<uint64_t>(src)));
 }
 
+// prefetch a contiguous global range into L2
 __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
                  : "memory");

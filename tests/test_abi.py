@@ -117,6 +117,74 @@ def test_binding_refuses_cpu_tensors():
         mla.mla_get_metadata(x, 16, 1, num_parts=3)
 
 
+class _NoLibrary:
+    """Stands in for the loaded library: any call through it fails the test."""
+
+    def __getattr__(self, name):
+        raise AssertionError(f"{name} was called although the arguments were invalid")
+
+
+def _cpu_binding(monkeypatch):
+    """The Python binding with its CUDA-device check relaxed to dtype and
+    contiguity (CPU tensors stand in for device ones) and no library behind it."""
+    import contextlib
+
+    import torch
+    from mla_decode_attention_latent_gb300 import api
+
+    def need(name, t, dtype):
+        if t.dtype != dtype or not t.is_contiguous():
+            raise TypeError(name)
+
+    monkeypatch.setattr(api, "_need_cuda", need)
+    monkeypatch.setattr(api, "load", lambda: _NoLibrary())
+    monkeypatch.setattr(api, "mla_workspace_bytes", lambda *a: 1 << 20)
+    monkeypatch.setattr(api, "_stream_handle", lambda dev: None)
+    monkeypatch.setattr(torch.cuda, "device", lambda dev: contextlib.nullcontext())
+    b, s_q, h_q = 2, 1, 16
+    t = dict(q=torch.zeros((b, s_q, h_q, 576), dtype=torch.bfloat16),
+             kcache=torch.zeros((4, 64, 1, 576), dtype=torch.bfloat16),
+             block_table=torch.zeros((b, 2), dtype=torch.int32), cache_seqlens=torch.zeros(b, dtype=torch.int32),
+             tile_scheduler_metadata=torch.zeros((3, 8), dtype=torch.int32),
+             num_splits=torch.zeros(b + 1, dtype=torch.int32),
+             out=torch.zeros((b, s_q, h_q, 512), dtype=torch.bfloat16), lse=torch.zeros((b, s_q, h_q)))
+    return api, t
+
+
+@pytest.mark.parametrize("entry", ["mla_decode_kvcache", "mla_decode_kvcache_noalloc"])
+@pytest.mark.parametrize("bad", ["out_rows", "out_dv", "lse", "num_splits", "metadata", "block_table", "kcache_page"])
+def test_binding_checks_shapes_before_the_library(monkeypatch, entry, bad):
+    # a too-small out / lse or a short num_splits would let the kernels read
+    # or write out of bounds: the binding must refuse them before any call
+    import torch
+    api, t = _cpu_binding(monkeypatch)
+    if bad == "out_rows":
+        t["out"] = torch.zeros((2, 1, 8, 512), dtype=torch.bfloat16)
+    elif bad == "out_dv":
+        t["out"] = torch.zeros((2, 1, 16, 256), dtype=torch.bfloat16)
+    elif bad == "lse":
+        t["lse"] = torch.zeros((2, 1))
+    elif bad == "num_splits":
+        t["num_splits"] = torch.zeros(2, dtype=torch.int32)
+    elif bad == "metadata":
+        t["tile_scheduler_metadata"] = torch.zeros((3, 4), dtype=torch.int32)
+    elif bad == "block_table":
+        t["block_table"] = torch.zeros((1, 2), dtype=torch.int32)
+    elif bad == "kcache_page":
+        t["kcache"] = torch.zeros((4, 32, 1, 576), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        getattr(api, entry)(t["q"], t["kcache"], t["block_table"], t["cache_seqlens"], 512,
+                            t["tile_scheduler_metadata"], t["num_splits"], out=t["out"], lse=t["lse"])
+
+
+def test_binding_reaches_the_library_with_good_shapes(monkeypatch):
+    # the same fixture with correct shapes gets past the checks (to the stand-in library)
+    api, t = _cpu_binding(monkeypatch)
+    with pytest.raises(AssertionError, match="mla_decode_kvcache_noalloc was called"):
+        api.mla_decode_kvcache_noalloc(t["q"], t["kcache"], t["block_table"], t["cache_seqlens"], 512,
+                                       t["tile_scheduler_metadata"], t["num_splits"], out=t["out"], lse=t["lse"])
+
+
 def _decode_fp8(lib, **over):
     a = dict(q=16, kv=16, num_blocks=4, bt=16, max_blocks=2, sl=16, batch=2, s_q=1, h_q=16, h_kv=1, d=576,
              dv=512, md=16, ns=16, num_parts=3, scale=1 / 24, causal=0, o=16, lse=16, ws=256, ws_bytes=1 << 30)

@@ -123,8 +123,10 @@ def test_scheduler_matches_oracle_partition():
 
 @pytest.mark.parametrize("batch,parts", [(9000, 152), (300, 600), (8191, 256), (8192, 257), (1, 1), (5, 1000)])
 def test_scheduler_large_batches_and_part_counts(batch, parts):
-    # past the scheduler's shared-memory staging (8192 sequences, 256 parts)
-    # the overflow goes straight to global memory; the partition must not change
+    # batches larger than the scheduler's 512 threads (each thread then owns a
+    # chunk of several sequences), chunk sizes that do not divide the batch,
+    # more parts than sequences, and a single part: the partition must equal
+    # the oracle's bit for bit
     import mla_decode_attention_latent_gb300 as mla
     rng = np.random.default_rng(batch + parts)
     sl = rng.integers(0, 5000, size=batch).astype(np.int32)

@@ -64,14 +64,36 @@ def test_noalloc_matches_regular_entry_point_twice(name, batch, s_q, h_q, seqlen
         assert _within_tolerance(o, lse, o_ref, lse_ref), f"call {call} differs from mla_decode_kvcache"
 
 
-def test_noalloc_rejects_shapes_beyond_its_scratch():
+def test_noalloc_scratch_limit_in_workspace_bytes():
+    # host only: the MTP-sized shape with 200 parts needs more scratch than the
+    # fixed array holds, while the uniform decode fits
     lib = _lib.load()
-    # 1024 query rows x (512 + 1) fp32 x (32 + 200) splits is far above the fixed scratch
-    need = lib.mla_workspace_bytes(32, 8, 128, 1, 512, 200)
-    assert need > _lib.MLA_NOALLOC_SCRATCH_BYTES
-    st = lib.mla_decode_kvcache_noalloc(16, 16, 4, 16, 2, 16, 32, 8, 128, 1, 576, 512, 16, 16, 200,
-                                        ctypes.c_float(1 / 24), 1, 16, 16, None)
-    assert st == _lib.MLA_ERR_WORKSPACE
-    st = lib.mla_decode_kvcache_noalloc(16, 16, 4, 16, 2, 16, 2, 1, 16, 1, 576, 256, 16, 16, 3,
-                                        ctypes.c_float(1 / 24), 0, 16, 16, None)
-    assert st == _lib.MLA_ERR_UNSUPPORTED
+    assert lib.mla_workspace_bytes(32, 8, 128, 1, 512, 200) > _lib.MLA_NOALLOC_SCRATCH_BYTES
+    assert 0 < lib.mla_workspace_bytes(64, 1, 128, 1, 512, 76) <= _lib.MLA_NOALLOC_SCRATCH_BYTES
+
+
+@pytest.mark.gpu
+def test_noalloc_rejects_shapes_beyond_its_scratch():
+    # every tensor is a real device buffer sized for the shape it claims (empty
+    # caches, so nothing would be read even if a launch happened): the refusal
+    # is checked without any pointer that a kernel could not use
+    import mla_decode_attention_latent_gb300 as mla
+    lib = _lib.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    for batch, s_q, h_q, d, dv, parts, want in ((32, 8, 128, 576, 512, 200, _lib.MLA_ERR_WORKSPACE),
+                                                (2, 1, 16, 576, 256, 3, _lib.MLA_ERR_UNSUPPORTED)):
+        q = torch.zeros((batch, s_q, h_q, d), dtype=torch.bfloat16, device=dev)
+        kc = torch.zeros((4, 64, 1, d), dtype=torch.bfloat16, device=dev)
+        bt = torch.zeros((batch, 2), dtype=torch.int32, device=dev)
+        sl = torch.zeros((batch,), dtype=torch.int32, device=dev)
+        md, ns = mla.mla_get_metadata(sl, s_q * h_q, 1, num_parts=parts)
+        o = torch.zeros((batch, s_q, h_q, max(dv, 512)), dtype=torch.bfloat16, device=dev)
+        lse = torch.zeros((batch, s_q, h_q), dtype=torch.float32, device=dev)
+        st = lib.mla_decode_kvcache_noalloc(q.data_ptr(), kc.data_ptr(), 4, bt.data_ptr(), 2, sl.data_ptr(), batch,
+                                            s_q, h_q, 1, d, dv, md.data_ptr(), ns.data_ptr(), parts,
+                                            ctypes.c_float(1 / 24), 1, o.data_ptr(), lse.data_ptr(), stream)
+        assert st == want, _lib.status_string(st)
+    torch.cuda.synchronize()
+    assert mla.mla_device_status(clear=True) == 0
