@@ -89,6 +89,8 @@ struct CUstream_st;
 #define MLA_DEVERR_TIMEOUT 0x1     /* a bounded wait inside a kernel gave up */
 #define MLA_DEVERR_BLOCK_ID 0x2    /* a block_table entry was outside [0, num_blocks) */
 #define MLA_DEVERR_SEQLEN 0x4      /* a cache_seqlens entry was negative or beyond the table */
+#define MLA_DEVERR_SCALE 0x8       /* an e4m3 page held a scale with |c| >= 255 (or NaN) for a token
+                                      inside its sequence (mla_decode_kvcache_fp8) */
 
 /*
  * mla_num_sm_parts — number of split-KV work parts for one decode call.
@@ -215,7 +217,11 @@ MLA_API int mla_decode_kvcache(const void *q, const void *kcache, int64_t num_bl
  * Precision: the kernel computes in f16 on the tensor cores.  The e4m3 codes
  * widen to f16 exactly; q is rounded to f16 (exact for |q| in [2^-17, 65504]);
  * the softmax weights times c_j are rounded to f16, so |c_j| must stay below
- * 255 (larger scales overflow; the call does not check the scales).
+ * 255 for every token inside a sequence (a larger one can overflow f16).  A
+ * scale with |c_j| >= 255, or a NaN scale, of a token inside its sequence
+ * sets MLA_DEVERR_SCALE in the device status word, and the outputs of that
+ * sequence are then undefined.  Scales of rows past a sequence's end are
+ * never read.
  * Stream order, graph capture and errors: as for mla_decode_kvcache.
  */
 #define MLA_FP8_PAGE_BYTES(d) (MLA_PAGE_SIZE * (d) + MLA_PAGE_SIZE * 4)

@@ -35,6 +35,7 @@ def MLA_FP8_PAGE_BYTES(d: int) -> int:
 MLA_DEVERR_TIMEOUT = 0x1
 MLA_DEVERR_BLOCK_ID = 0x2
 MLA_DEVERR_SEQLEN = 0x4
+MLA_DEVERR_SCALE = 0x8
 
 # every call the C header declares, with its ctypes signature
 _P, _I, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float

@@ -129,6 +129,7 @@ constexpr uint32_t kE4ScaleOff = kPage * kD;               // the scales' byte o
 constexpr uint32_t kE4ChunkBytes = kPage * 64;             // one 64-dim chunk of one page: 4 KB of codes
 constexpr uint32_t kLandBytes = 2 * kE4ChunkBytes;         // a landing buffer: one chunk of two pages (8 KB)
 constexpr uint32_t kVLandOff = kVStageBytes / 2;           // e4m3 page landing inside a V stage (upper 32 KB)
+constexpr float kE4ScaleLimit = 255.f;                     // |scale| bound: P (< 2^8) times it stays in f16 range
 constexpr int kScSlots = 8;                                // scale ring: one slot per step of two pages (a producer
                                                            // waits on the rows of 8 steps back: never in practice)
 constexpr uint32_t kScBytes = 2 * kPage * 4;               // 512 B
@@ -845,6 +846,17 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
             const int scs = (int)(step % kScSlots);  // e4m3: this step's slot in the scale ring
             if (q2 == 0 && !warp_wait(c, B_SFULL + sb, (step / kSBufs) & 1)) return;
             if (kRing && q2 == 0 && !warp_wait(c, B_SCFULL + scs, (step / kScSlots) & 1)) return;
+            if (kFp8 && (warp & 3) == 0) {
+                // one warp checks the scales of the sequence's tokens on this
+                // page against the f16 limit, lane i tokens i and i + 32 (a
+                // NaN scale fails the test too)
+                const uint32_t sc_s = smem_u32(c.base + kScaleOff) + (uint32_t)scs * kScBytes + (uint32_t)q2 * kPage * 4;
+                const int nseq = min(kPage, s.T - pg * kPage);
+                const float a = lane < nseq ? fabsf(__uint_as_float(lds32(sc_s + 4 * lane))) : 0.f;
+                const float b = lane + 32 < nseq ? fabsf(__uint_as_float(lds32(sc_s + 4 * (lane + 32)))) : 0.f;
+                if (__any_sync(0xffffffffu, !(a < kE4ScaleLimit) || !(b < kE4ScaleLimit)) && lane == 0)
+                    atomicOr(p.status, MLA_DEVERR_SCALE);
+            }
             tc_fence_after();
             uint32_t sr[64];
             {

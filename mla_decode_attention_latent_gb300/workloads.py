@@ -166,6 +166,61 @@ def make_inputs(case: Case, device: str = "cpu", seqlens: Optional[Sequence[int]
     return Inputs(case, q, kcache, bt.to(device), sl.to(device), indices)
 
 
+def staircase(x: Inputs, level_starts: Sequence[int], jump_log2: float = 11.0, max_exp: float = 40.0,
+              seed: int = 0) -> Inputs:
+    """Inputs whose attention scores climb in steps along each sequence.
+
+    Key t of sequence b sits on level v(t) = the number of ``level_starts`` at
+    or below its page (for a sparse case: the 64-entry chunk of the first query
+    token's list that holds it).  Only 64 "score dims" of q are nonzero (the
+    RoPE dims 512..575 when d = 576, else dims 0..63); there every key holds
+    2 v(t) plus N(0, 0.5) noise and head h of q holds a gain g_h plus N(0, 0.05)
+    noise, with g_h spread over +-5 % around jump_log2 / (2 * 64 * log2(e) / sqrt(d)),
+    so that at softmax scale 1/sqrt(d) each level raises the scores by about
+    ``jump_log2`` in log2 units.  Every other dim of a key is N(0, 1) times
+    2^(jump_log2 * (top - v(t))), capped at 2^max_exp, where top is the highest
+    level of the key's sequence: the lower weight of an older key is made up
+    by a larger value row, so every level carries a visible share of O, and O
+    stays of order one.  Returns new Inputs (the table, lengths and lists are
+    kept); e4m3 cases are re-quantized per token."""
+    c = x.case
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(c.seed * 7919 + seed + 13)
+    sl = x.cache_seqlens.cpu().tolist()
+    bt = x.block_table.cpu()
+    n_pool = x.kcache.shape[0]
+    starts = sorted(int(v) for v in level_starts)
+    sd = slice(D_V, c.d) if c.d > D_V else slice(0, 64)   # the score dims
+    rows = torch.randn((n_pool, c.page, c.d), generator=gen, dtype=torch.float32)
+    for b, T in enumerate(sl):
+        if x.indices is not None:
+            lvl_of = torch.zeros(int(T), dtype=torch.int64)   # positions outside the list stay on level 0
+            lst = x.indices[b, 0].cpu().long()
+            for e, pos in enumerate(lst.tolist()):
+                if 0 <= pos < T:
+                    lvl_of[pos] = sum(1 for v in starts if v <= e // c.page) - 1
+        else:
+            lvl_of = torch.tensor([sum(1 for v in starts if v <= t // c.page) - 1 for t in range(int(T))],
+                                  dtype=torch.int64)
+        lvl_of = lvl_of.clamp(min=0)
+        top = int(lvl_of.max()) if int(T) > 0 else 0   # the sequence's own highest level
+        for t in range(int(T)):
+            blk, r = int(bt[b, t // c.page]), t % c.page
+            v = int(lvl_of[t])
+            rows[blk, r] *= 2.0 ** min(max_exp, jump_log2 * (top - v))
+            rows[blk, r, sd] = 2.0 * v + 0.5 * torch.randn(64, generator=gen)
+    gain = jump_log2 / (2 * 64 * math.log2(math.e) / math.sqrt(c.d))
+    g = gain * (0.95 + 0.1 * torch.arange(c.h_q, dtype=torch.float32) / c.h_q)
+    q = torch.zeros((c.batch, c.s_q, c.h_q, c.d), dtype=torch.float32)
+    q[..., sd] = g[None, None, :, None] + 0.05 * torch.randn((c.batch, c.s_q, c.h_q, 64), generator=gen)
+    if c.fp8:
+        kcache = pack_e4m3_pages(rows)
+    else:
+        kcache = rows[:, :, None, :].to(torch.bfloat16)
+    dev = x.q.device
+    return Inputs(c, q.to(torch.bfloat16).to(dev), kcache.to(dev), x.block_table, x.cache_seqlens, x.indices)
+
+
 def valid_list_entries(case: Case, seqlens: Sequence[int]) -> int:
     """Valid entries over all index lists of a sparse case (``make_index_lists``
     lists hold min(topk, T_b) distinct positions per query token)."""

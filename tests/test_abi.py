@@ -37,7 +37,7 @@ def test_header_constants_match_binding():
     text = open(HEADER).read()
     for name in ("MLA_OK", "MLA_ERR_INVALID_ARG", "MLA_ERR_UNSUPPORTED", "MLA_ERR_WORKSPACE", "MLA_ERR_CUDA",
                  "MLA_ERR_DEVICE", "MLA_PAGE_SIZE", "MLA_HEAD_DIM", "MLA_V_DIM", "MLA_METADATA_INTS",
-                 "MLA_DEVERR_TIMEOUT", "MLA_DEVERR_BLOCK_ID", "MLA_DEVERR_SEQLEN"):
+                 "MLA_DEVERR_TIMEOUT", "MLA_DEVERR_BLOCK_ID", "MLA_DEVERR_SEQLEN", "MLA_DEVERR_SCALE"):
         m = re.search(rf"#define {name} \(?(-?0x[0-9a-fA-F]+|-?\d+)\)?", text)
         assert m, name
         assert int(m.group(1), 0) == getattr(_lib, name), name

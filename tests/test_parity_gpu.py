@@ -307,6 +307,29 @@ def test_fp8_garbage_past_the_end():
     check(c, mutate=poison)
 
 
+@pytest.mark.parametrize("bad", [300.0, -255.0, float("nan")])
+def test_fp8_scale_beyond_the_limit_is_reported(bad):
+    # a token inside a sequence whose scale is at or above 255 in magnitude (or
+    # NaN) sets MLA_DEVERR_SCALE; the same scale past a sequence's end does not
+    import mla_decode_attention_latent_gb300 as mla
+    scale_off = 64 * 576
+    c = fp8_case("fp8-scale", 2, 1, 32, [100, 37], seed=132, pool_pages=6)
+    x = W.make_inputs(c, "cpu")
+    tail_page = int(x.block_table[1, 0])
+    x.kcache[tail_page, scale_off + 4 * 50:scale_off + 4 * 51] = torch.tensor([bad], dtype=torch.float32).view(torch.uint8)
+    o_ref, lse_ref = oracle_of(x)
+    o, lse, _, _, st = run_gpu(to_device(x, DEV))
+    assert st == 0, f"a scale past the end was reported: {st:#x}"
+    assert_parity(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "scale past the end")
+    inside = int(x.block_table[0, 1])          # token 64 + 7 of the first sequence
+    x.kcache[inside, scale_off + 4 * 7:scale_off + 4 * 8] = torch.tensor([bad], dtype=torch.float32).view(torch.uint8)
+    mla.mla_device_status(clear=True)
+    o, lse, _, _, st = run_gpu(to_device(x, DEV))
+    assert st & _lib.MLA_DEVERR_SCALE, f"status {st:#x}"
+    # the other sequence is unaffected
+    assert_parity(o[1].float().cpu().numpy(), lse[1].cpu().numpy(), o_ref[1], lse_ref[1], "other sequence")
+
+
 def test_fp8_deterministic_and_split_invariant():
     c = fp8_case("fp8-det", 2, 1, 128, [3000, 1500], seed=131)
     x = to_device(W.make_inputs(c, "cpu"), DEV)
