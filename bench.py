@@ -4,8 +4,10 @@
 
 One step is one pass of the whole path over one batch: the tile scheduler
 (mla_get_metadata), the split-KV kernel and the combine (mla_decode_kvcache),
-on inputs already resident in HBM.  The default workload is the uniform decode
-batch (b=64, s_q=1, h_q=128, 4096 cached tokens per sequence, page 64).
+on inputs already resident in HBM.  The default workload is the largest
+single-GPU one, the long-context decode batch (b=64, s_q=1, h_q=128, 65536
+cached tokens per sequence, page 64: 4.85 GB of KV pages).  --workload all
+prints one line for every workload, in turn.
 
 Reported figures (one JSON line from rank 0):
   value         KV-cache GB/s: bytes of the KV pages touched plus q, O and LSE,
@@ -14,6 +16,9 @@ Reported figures (one JSON line from rank 0):
   tflops        2 * h_q * (576 + 512) * visible keys, per second
   roofline      the split-KV kernel alone (CUDA events around it on its stream)
                 against the measured HBM copy bandwidth
+  decode_only   the same metric for the decode call alone (split-KV + combine),
+                with the metadata computed once and reused, as every layer
+                of a model reuses it
   e2e           the same metric through the public API with host buffers:
                 pinned host -> device copies of every input, the two calls,
                 device -> host copies of O and LSE, all inside the timed region
@@ -302,7 +307,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="uniform")
+    ap.add_argument("--workload", default="long", help="a workload name, or 'all'")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -311,16 +316,37 @@ def main():
         args.warmup = 3
 
     from mla_decode_attention_latent_gb300 import workloads as W
-    case = W.CASES[args.workload]
+    names = ALL_WORKLOADS if args.workload == "all" else [args.workload]
 
     if args.impl == "reference":
-        return reference_arm(args, case)
+        for name in names:
+            reference_arm(args, W.CASES[name])
+        return
 
     rank, world, local = dist_setup(args.gpus)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     import mla_decode_attention_latent_gb300 as mla
     mla._lib.load()
+    for name in names:
+        line = run_workload(args, mla, W.CASES[name], name, rank, world, local, dev)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        torch.cuda.empty_cache()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+L2_FLUSH_BYTES = 256 << 20  # twice the GB300's L2
+
+# every workload, in the order --workload all runs them
+ALL_WORKLOADS = ["tiny", "uniform", "variable", "mtp", "long", "uniform_d512", "uniform_fp8", "sparse"]
+
+
+def run_workload(args, mla, case, name, rank, world, local, dev):
+    """Time one workload; returns rank 0's JSON line (None on other ranks)."""
+    from mla_decode_attention_latent_gb300 import workloads as W
     case = rank_case(case, rank)
 
     x = W.make_inputs(case, device=str(dev))
@@ -340,8 +366,9 @@ def main():
 
     decode = mla.mla_decode_kvcache_fp8 if case.fp8 else mla.mla_decode_kvcache
 
-    def step():
-        md_k, ns_k = mla.mla_get_metadata(part_lens, case.num_q_rows, case.h_kv, num_parts=num_parts)
+    def step(md_k=None, ns_k=None):
+        if md_k is None:
+            md_k, ns_k = mla.mla_get_metadata(part_lens, case.num_q_rows, case.h_kv, num_parts=num_parts)
         if case.topk:
             mla.mla_decode_kvcache_sparse(x.q, x.kcache, x.block_table, x.cache_seqlens, x.indices, case.dv, md_k,
                                           ns_k, list_lens=part_lens, softmax_scale=case.softmax_scale, out=o, lse=lse,
@@ -360,8 +387,31 @@ def main():
     for a, b in ev_split:
         a.record(stream)
         b.record(stream)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+
+    # a workload whose bytes fit in L2 is timed step by step, with L2 flushed
+    # (a 256 MB buffer written) between steps, outside the timed intervals
+    small = fig["bytes"] < L2_FLUSH_BYTES
+    flush = torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=dev) if small else None
+
+    def timed(fn):
+        """ms of args.steps calls of fn: back to back, or one by one with L2 flushed between them."""
+        if not small:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(args.steps):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b)
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for a, b in pairs:
+            flush.zero_()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in pairs)
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -369,27 +419,36 @@ def main():
     # between their kernels, so each launch may overlap its predecessor's tail
     barrier(world)
     torch.cuda.synchronize()
-    start.record(stream)
-    for k in range(args.steps):
-        step()
-    end.record(stream)
-    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("steps")
+    ms_total = timed(step)
+    torch.cuda.nvtx.range_pop()
     barrier(world)
     assert mla.mla_device_status(clear=True) == 0, "device-side error in the timed region"
-    ms_total = start.elapsed_time(end)
     # timed region 2 (roofline): the same K steps with CUDA events around each
     # split-KV launch on its stream; the events cost several us per step, which
     # is why they stay out of region 1
     barrier(world)
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("steps_with_split_events")
     for k in range(args.steps):
         mla.mla_set_timing_events(*ev_split[k])
         step()
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     barrier(world)
     mla.mla_set_timing_events(None, None)
+    # timed region 3 (decode_only): the decode call alone, with the metadata
+    # of the first step reused by every later one (as every layer reuses it)
+    md_once, ns_once = mla.mla_get_metadata(part_lens, case.num_q_rows, case.h_kv, num_parts=num_parts)
+    barrier(world)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("decode_only")
+    ms_decode = timed(lambda: step(md_once, ns_once))
+    torch.cuda.nvtx.range_pop()
+    barrier(world)
     clk = clocks.stop()
     assert mla.mla_device_status(clear=True) == 0, "device-side error in the timed region"
+    ms_decode = max_over_ranks(ms_decode, world) / args.steps
 
     ms_total = max_over_ranks(ms_total, world)
     ms_step = ms_total / args.steps
@@ -398,7 +457,7 @@ def main():
     tflops = fig["flops"] * world / (ms_step * 1e-3) / 1e12
     pk = peaks()
     bound, achieved, peak, unit = roofline(fig, split_ms, pk)
-    traffic = split_kernel_traffic(args.workload)
+    traffic = split_kernel_traffic(name)
 
     # end-to-end through the public API with host buffers
     e2e = None
@@ -428,21 +487,23 @@ def main():
             "config": {"workload": workload_label(case),
                        "batch": case.batch, "s_q": case.s_q, "h_q": case.h_q, "num_parts": num_parts,
                        "kv_bytes": fig["kv_bytes"], "bytes_per_call": fig["bytes"], "flops_per_call": fig["flops"],
-                       "l2": "no flush: KV pages touched per call exceed the 129 MB L2",
+                       "l2": ("flushed between steps (256 MB written), per-step events" if small else
+                              "no flush: the bytes of a call exceed the 129 MB L2"),
                        "parallelism": f"replicas x{world}, one batch per GPU" if world > 1 else "single GPU"},
             "roofline": {"bound": bound, "kernel": "split_kv", "achieved": round(achieved, 1),
                          "peak": peak, "unit": unit, "frac": round(achieved / peak, 4),
                          "peak_source": pk["source"], "split_kernel_ms": round(split_ms, 5),
                          "traffic": traffic},
+            "decode_only": {"us_per_call": round(ms_decode * 1e3, 2),
+                            "value": round(aggregate_gbs(fig["bytes"], world, ms_decode), 2), "unit": "GB/s",
+                            "what": "split-KV + combine per call, metadata computed once and reused"},
             "clocks": clk,
             "e2e": e2e,
             "gpu_launches": 3 * args.steps,
             "cpu_baseline": cpu,
         }
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+        return line
+    return None
 
 
 def e2e_run(mla, case, x, fig, dev, stream, steps, world):

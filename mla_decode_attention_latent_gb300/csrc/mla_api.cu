@@ -1,6 +1,7 @@
 // C ABI of the MLA decode library: argument validation, workspace layout and
 // kernel launches.  See include/mla_decode.h for the contract of each call.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <mutex>
 
@@ -29,6 +30,14 @@ int status_address(unsigned int **out) {
     *out = g_status_addr[dev];
     return MLA_OK;
 }
+
+// NVTX range over a call's host side (argument checks and launches), so that
+// a profiler timeline ties the kernels to the call that enqueued them; free
+// when no tool is attached
+struct Range {
+    explicit Range(const char *name) { nvtxRangePushA(name); }
+    ~Range() { nvtxRangePop(); }
+};
 
 constexpr size_t kAlign = 256;
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -84,6 +93,7 @@ int mla_get_metadata(const int32_t *cache_seqlens, int batch, int num_q_rows, in
     if (!cache_seqlens || !tile_scheduler_metadata || !num_splits) return MLA_ERR_INVALID_ARG;
     if (batch < 1 || num_q_rows < 1 || h_kv < 1 || num_parts < 1) return MLA_ERR_INVALID_ARG;
     if (h_kv != 1) return MLA_ERR_UNSUPPORTED;
+    Range range("mla_get_metadata");
     unsigned int *status = nullptr;
     if (status_address(&status) != MLA_OK) return MLA_ERR_CUDA;
     cudaError_t e = launch_schedule(cache_seqlens, batch, num_parts, tile_scheduler_metadata, num_splits, status,
@@ -119,6 +129,7 @@ int decode(const void *q, const void *kcache, Kind kind, int64_t num_blocks, con
            int causal, void *o, float *lse, void *workspace, size_t ws_bytes, struct CUstream_st *stream,
            const Lists &lists = Lists()) {
     const bool e4m3 = kind == Kind::kE4m3, sparse = kind == Kind::kSparse;
+    Range range(sparse ? "mla_decode_kvcache_sparse" : e4m3 ? "mla_decode_kvcache_fp8" : "mla_decode_kvcache");
     if (!q || !kcache || !block_table || !cache_seqlens || !tile_scheduler_metadata || !num_splits || !o || !lse ||
         !workspace)
         return MLA_ERR_INVALID_ARG;

@@ -307,8 +307,8 @@ __device__ __forceinline__ bool widen_e4m3(uint32_t base, uint32_t land, int tid
 // taking the steps of parity r).  A step is up to two consecutive pages
 // of a segment; each of a step's 9 64-dim chunks is one 16 KB ring slot
 // holding 128 token rows (first page rows 0-63, second page rows 64-127), so
-// that one tcgen05 MMA with N = 128 covers both pages.  Producer 0 first asks
-// L2 for the Q rows of every segment.  (Streaming whole pages into L2 ahead
+// that one tcgen05 MMA with N = 128 covers both pages.  Producer 0 asks L2 for
+// each segment's Q rows as it reaches the segment.  (Streaming whole pages into L2 ahead
 // of the chunk loads, from either CTA and at any distance tried, measured
 // slower on GB300 than letting the chunk loads fetch them.)
 __device__ void score_producer(const DecodeParams &p, const Ctx &c, const CUtensorMap *map, int part, int tile,
@@ -324,18 +324,17 @@ __device__ void score_producer(const DecodeParams &p, const Ctx &c, const CUtens
         if (bb >= 0 && bb < p.batch && bp >= 0 && bp < p.max_blocks)
             prefetch_line_l1(p.block_table + (size_t)bb * p.max_blocks + bp);
     }
-    if (r == 0) {
-        const int rows = min(kTileRows, p.rows - tile * kTileRows);
-        walk.init(p, part);
-        while (walk.next(p, s))
-            if (s.p1 > s.p0 && rows > 0)
-                prefetch_l2(p.q + ((size_t)s.b * p.rows + (size_t)tile * kTileRows) * kD, (uint32_t)rows * kD * 2);
-    }
+    const int rows = min(kTileRows, p.rows - tile * kTileRows);
     walk.init(p, part);
     uint32_t ring_it = 0;  // chunks issued into this producer's ring
     uint32_t step = 0;
     bool ok = true;
     while (ok && walk.next(p, s)) {
+        // producer 0 asks L2 for the segment's Q rows as it reaches the
+        // segment, a few pages before the row warps load them (a prefetch at
+        // the part's start would be evicted by the pages streamed meanwhile)
+        if (r == 0 && s.p1 > s.p0 && rows > 0)
+            prefetch_l2(p.q + ((size_t)s.b * p.rows + (size_t)tile * kTileRows) * kD, (uint32_t)rows * kD * 2);
         for (int pg = s.p0; ok && pg < s.p1; pg += 2, ++step) {
             const int npg = min(2, s.p1 - pg);
             if ((int)(step % kScoreIssuers) != r) continue;  // the other ring's step
@@ -796,14 +795,32 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
         if (s.p1 > s.p0) {
             // Q row r: latent dims 0..511 into TMEM lane r (columns 0..255,
             // bf16 pairs, or f16 pairs for the e4m3 cache), RoPE dims 512..575
-            // into row r of the swizzled smem tile; four 64-dim chunks (32
-            // loads) in flight at a time
+            // into row r of the swizzled smem tile.  Two rounds of loads: the
+            // RoPE chunk with latent chunks 0..3 (40 loads in flight), then
+            // chunks 4..7.
             const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q + ((size_t)s.b * p.rows + (row_ok ? gr : 0)) * kD);
+            uint4 y[kHasRope ? 8 : 1];
+            if constexpr (kHasRope) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) y[j] = row_ok ? __ldg(qrow + kLatChunks * 8 + j) : make_uint4(0, 0, 0, 0);
+            }
 #pragma unroll 1
             for (int ch0 = 0; ch0 < kLatChunks; ch0 += 4) {
                 uint4 x[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) x[j] = row_ok ? __ldg(qrow + ch0 * 8 + j) : make_uint4(0, 0, 0, 0);
+                if (kHasRope && ch0 == 0) {
+                    const uint32_t rope = smem_u32(c.base + kQRopeOff) + (uint32_t)r * 128u;
+#pragma unroll
+                    for (int j = 0; j < (kHasRope ? 8 : 0); ++j) {
+                        uint4 v = y[j];
+                        if constexpr (kFp8)
+                            v = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                                           bf16x2_to_f16x2(v.w));
+                        sts128(rope + 16u * (uint32_t)(j ^ (r & 7)), v.x, v.y, v.z, v.w);
+                    }
+                    fence_proxy_async_smem();
+                }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     uint32_t v[32];
@@ -820,18 +837,6 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
                     }
                     tmem_st32(tmem + lane_base + (ch0 + k) * 32, v);
                 }
-            }
-            if constexpr (kHasRope) {
-                uint4 *rope = reinterpret_cast<uint4 *>(c.base + kQRopeOff + r * 128);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    uint4 y = row_ok ? __ldg(qrow + kLatChunks * 8 + j) : make_uint4(0, 0, 0, 0);
-                    if constexpr (kFp8)
-                        y = make_uint4(bf16x2_to_f16x2(y.x), bf16x2_to_f16x2(y.y), bf16x2_to_f16x2(y.z),
-                                       bf16x2_to_f16x2(y.w));
-                    rope[j ^ (r & 7)] = y;
-                }
-                fence_proxy_async_smem();
             }
             tmem_wait_st();
         }

@@ -86,7 +86,9 @@ def sampled_oracle(x: W.Inputs, seqs, rows_per_seq, rng):
 
     Only the pages of the sampled sequences are copied to the host (as a
     compact pool with a remapped block table), so multi-GB caches stay on the
-    device.  Returns (flat row ids into the full output, o_ref, lse_ref).
+    device; index lists (sparse decode) keep their positions, which the
+    remapped table resolves.  Returns (flat row ids into the full output,
+    o_ref, lse_ref).
     """
     c = x.case
     sl = x.cache_seqlens.cpu().numpy()
@@ -112,6 +114,11 @@ def sampled_oracle(x: W.Inputs, seqs, rows_per_seq, rng):
         for r in sorted(pick):
             local_rows.append(i * R + r)
             full_rows.append(b * R + r)
-    o_ref, lse_ref = _oracle_call(c, q, kc, bt_c, sl[list(seqs)].astype(np.int32),
-                                  rows=np.array(local_rows, np.int64))
+    rows = np.array(local_rows, np.int64)
+    if x.indices is not None:
+        idx = x.indices[torch.as_tensor(list(seqs), device=x.indices.device)].cpu().numpy()
+        o_ref, lse_ref = oracle.mla_decode_sparse(W.bf16_bits(q), W.bf16_bits(kc), bt_c, sl[list(seqs)].astype(np.int32),
+                                                  idx, c.dv, c.softmax_scale, rows=rows)
+    else:
+        o_ref, lse_ref = _oracle_call(c, q, kc, bt_c, sl[list(seqs)].astype(np.int32), rows=rows)
     return np.array(full_rows, np.int64), o_ref, lse_ref

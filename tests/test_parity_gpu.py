@@ -229,16 +229,29 @@ def test_empty_segments_between_full_ones():
             assert torch.equal(o, o2) and torch.equal(lse, l2), parts
 
 
-@pytest.mark.parametrize("name", ["uniform", "variable", "mtp", "long", "uniform_d512", "uniform_fp8"])
+def run_gpu_sparse(x):
+    """The sparse decode as the benchmark launches it: partition on topk-long lists."""
+    import mla_decode_attention_latent_gb300 as mla
+    c = x.case
+    lens = torch.full((c.batch,), c.topk, dtype=torch.int32, device=x.q.device)
+    md, ns = mla.mla_get_metadata(lens, c.num_q_rows, c.h_kv)
+    o, lse = mla.mla_decode_kvcache_sparse(x.q, x.kcache, x.block_table, x.cache_seqlens, x.indices, c.dv, md, ns,
+                                           list_lens=lens, softmax_scale=c.softmax_scale)
+    torch.cuda.synchronize()
+    return o, lse, md, ns, mla.mla_device_status(clear=True)
+
+
+@pytest.mark.parametrize("name", ["uniform", "variable", "mtp", "long", "uniform_d512", "uniform_fp8", "sparse"])
 def test_full_size_repeatable(name):
     # bit-identical outputs over repeated launches at full size: every wait
     # on the hand-offs between the two CTAs of a pair has to be exact
     c = W.CASES[name]
     x = W.make_inputs(c, device="cuda")
-    o1, l1, _, _, st = run_gpu(x)
+    run = run_gpu_sparse if c.topk else run_gpu
+    o1, l1, _, _, st = run(x)
     assert st == 0, f"device status {st:#x}"
     for rep in range(4):
-        o2, l2, _, _, st = run_gpu(x)
+        o2, l2, _, _, st = run(x)
         assert st == 0, f"device status {st:#x}"
         n_o = int((o1.view(torch.int16) != o2.view(torch.int16)).sum())
         assert n_o == 0 and torch.equal(l1, l2), f"repeat {rep}: {n_o} O elements differ"
@@ -246,11 +259,11 @@ def test_full_size_repeatable(name):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("name", ["uniform", "variable", "mtp", "long", "uniform_d512", "uniform_fp8"])
+@pytest.mark.parametrize("name", ["uniform", "variable", "mtp", "long", "uniform_d512", "uniform_fp8", "sparse"])
 def test_full_size_sampled(name):
     c = W.CASES[name]
     x = W.make_inputs(c, device="cuda")
-    o, lse, _, _, st = run_gpu(x)
+    o, lse, _, _, st = run_gpu_sparse(x) if c.topk else run_gpu(x)
     assert st == 0, f"device status {st:#x}"
     rng = np.random.default_rng(123)
     seqs = sorted(rng.choice(c.batch, size=min(6, c.batch), replace=False).tolist())
