@@ -259,7 +259,9 @@ MLA_API int mla_decode_kvcache_fp8(const void *q, const void *kv_pages, int64_t 
  *                  every sequence)
  * A 128-row tile holds one query token's heads: s_q must be 1, or h_q 128
  * (MLA_ERR_UNSUPPORTED otherwise).  Rows are gathered one by one from the
- * cache, so any positions may be listed.
+ * cache (TMA gathers over the cache viewed as num_blocks * 64 rows, which
+ * must stay below 2^31: MLA_ERR_UNSUPPORTED otherwise), so any positions may
+ * be listed.
  * Stream order, graph capture and errors: as for mla_decode_kvcache.
  */
 MLA_API int mla_decode_kvcache_sparse(const void *q, const void *kcache, int64_t num_blocks,

@@ -143,6 +143,8 @@ int decode(const void *q, const void *kcache, Kind kind, int64_t num_blocks, con
         if (!lists.indices || !lists.list_lens || lists.topk < 1) return MLA_ERR_INVALID_ARG;
         // a 128-row tile must hold the heads of one query token
         if (d != kDqk || (s_q > 1 && h_q != kRowsPerTile)) return MLA_ERR_UNSUPPORTED;
+        // the gathers address cache rows with 32-bit coordinates
+        if (num_blocks > 0x7fffffffLL / kPage) return MLA_ERR_UNSUPPORTED;
     }
     if ((long long)s_q * h_q > kMaxRows) return MLA_ERR_UNSUPPORTED;
     if ((long long)max_blocks_per_seq * kPage > 0x7fffffffLL) return MLA_ERR_INVALID_ARG;

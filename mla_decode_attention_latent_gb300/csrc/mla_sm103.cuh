@@ -151,6 +151,18 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// gather of four rows of a 2-D tensor (box: 1 row of 64 elements): rows y0..y3
+// at column x land one after another at dst (128 B each with a 128-byte
+// swizzle), completing tx bytes on `bar`; a row past the tensor reads zeros
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, uint64_t *bar, int x, int y0, int y1,
+                                            int y2, int y3) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+        "%3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // bulk copy of `bytes` from this CTA's shared memory into a peer CTA's shared
 // memory; completes the transaction bytes on the peer's barrier
 __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const void *src, uint32_t bytes,
@@ -169,22 +181,6 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
                      smem_u32(dst)),
                  "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
                  : "memory");
-}
-
-// 16-byte asynchronous copy global -> this CTA's shared memory (cp.async,
-// cached in L2 only); src_bytes = 0 writes 16 zero bytes and reads nothing.
-// Both addresses 16-byte aligned.  Completion: cp_async_commit / cp_async_wait.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)),
-                 "r"(src_bytes)
-                 : "memory");
-}
-// close this thread's group of cp.async copies
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// wait until at most N of this thread's most recent groups are still in flight
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // bring the line holding `src` into L1 (no register result, never faults)

@@ -471,55 +471,68 @@ __device__ void score_producer_e4m3(const DecodeParams &p, const Ctx &c, const C
 // A part walks list chunks instead of pages: "page" pg of sequence b is list
 // entries 64 pg .. 64 pg + 63 of the tile's query token, and entry e names a
 // token position; positions outside [0, kv_lens[b]) and entries past the
-// list's length are invalid.  Row t of a 64-entry chunk is gathered from the
-// cache row of its position with 16-byte cp.async copies written straight
-// into the 128-byte-swizzled operand layout; an invalid row is zero-filled
-// (its score column is masked by the row warps, its V row contributes 0).
-
-// the cache row of list entry e (or nullptr when the entry is invalid)
-__device__ __forceinline__ const uint8_t *sparse_row(const DecodeParams &p, const int32_t *list, int list_len, int T,
-                                                     int b, int e) {
-    if (e >= list_len) return nullptr;
-    const int pos = list[e];
-    if (pos < 0 || pos >= T) return nullptr;
-    const int blk = p.block_table[(size_t)b * p.max_blocks + pos / kPage];
-    if (blk < 0 || (int64_t)blk >= p.num_blocks) {
-        atomicOr(p.status, MLA_DEVERR_BLOCK_ID);
-        return nullptr;
-    }
-    return reinterpret_cast<const uint8_t *>(p.kcache) + ((size_t)blk * kPage + pos % kPage) * (kD * 2);
-}
+// list's length are invalid.  Rows are gathered with TMA four at a time
+// (tile::gather4 over the cache viewed as a 2-D tensor of 64 num_blocks rows
+// of d elements), straight into the 128-byte-swizzled operand layout; an
+// invalid entry is given the row just past the cache, which the gather reads
+// as zeros (its score column is masked by the row warps, its V row adds 0).
 
 __device__ __forceinline__ int sparse_cache_len(const DecodeParams &p, int b) {
     int T = p.kv_lens[b];
     return T < 0 ? 0 : (T > p.max_blocks * kPage ? p.max_blocks * kPage : T);
 }
 
-// Score-CTA producer of the sparse decode; the whole warp runs it.  Lane l
-// gathers rows l, l + 32 (first list chunk of the step) and l + 64, l + 96
-// (second), 8 copies per row and 64-dim chunk; each chunk's copies are one
-// cp.async group, handed to the MMA issuer (B_KFULL) once complete, kGatherLag
-// chunks later.  The validity masks of the step's two list chunks go to the
-// side ring for the row warps.
-constexpr int kGatherLag = 4;
-static_assert(!kSparse || kGatherLag < kRingSlots, "a chunk is handed over before its slot is needed again");
-__device__ void score_producer_sparse(const DecodeParams &p, const Ctx &c, int part, int tile, int r) {
+// Cache rows of list entries e0 .. e0 + 3 of `list` (y[j], or the row past the
+// cache), and bit j of the result set when entry e0 + j is valid.  Lanes with
+// `on` false get four invalid entries.
+__device__ __forceinline__ uint32_t sparse_rows(const DecodeParams &p, const int32_t *list, int list_len, int T, int b,
+                                               int e0, bool on, int (&y)[4]) {
+    const int past = (int)(p.num_blocks * kPage);
+    int pos[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) pos[j] = (on && e0 + j < list_len) ? list[e0 + j] : -1;
+    uint32_t valid = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        y[j] = past;
+        if (pos[j] >= 0 && pos[j] < T) {
+            const int blk = p.block_table[(size_t)b * p.max_blocks + pos[j] / kPage];
+            if (blk < 0 || (int64_t)blk >= p.num_blocks) {
+                atomicOr(p.status, MLA_DEVERR_BLOCK_ID);
+            } else {
+                y[j] = blk * kPage + pos[j] % kPage;
+                valid |= 1u << j;
+            }
+        }
+    }
+    return valid;
+}
+
+// bit i of x (i < 16) to bit 4 i
+__device__ __forceinline__ uint64_t spread4(uint32_t x) {
+    uint64_t v = x & 0xFFFFu;
+    v = (v | (v << 24)) & 0x000000FF000000FFull;
+    v = (v | (v << 12)) & 0x000F000F000F000Full;
+    v = (v | (v << 6)) & 0x0303030303030303ull;
+    v = (v | (v << 3)) & 0x1111111111111111ull;
+    return v;
+}
+
+// Score-CTA producer of the sparse decode; the whole warp runs it.  The
+// step's 128 operand rows are list entries 64 pg .. 64 pg + 127; lane i
+// resolves entries 4 i .. 4 i + 3 (lanes 0..15 only for a one-page step) and
+// issues their gather for each 64-dim chunk into the chunk's ring slot, lane 0
+// having armed the slot's barrier with the chunk's bytes.  The validity masks
+// of the step's two list chunks go to the side ring for the row warps.  (The
+// gathers run at the TMA engine's rate for 128-byte row pieces, about
+// 10 GB/s per SM on GB300, which bounds this decode; looking the rows up
+// further ahead, or asking L2 for whole rows first, measured no faster.)
+__device__ void score_producer_sparse(const DecodeParams &p, const Ctx &c, const CUtensorMap *map, int part, int tile,
+                                      int r) {
     const int lane = threadIdx.x & 31;
     const int qtok = p.s_q == 1 ? 0 : tile;  // the tile's query token (h_q = 128 when s_q > 1)
     PartWalk walk;
     Segment s;
-    if (lane == 0 && r == 0) {
-        const int rows = min(kTileRows, p.rows - tile * kTileRows);
-        walk.init(p, part);
-        while (walk.next(p, s))
-            if (s.p1 > s.p0 && rows > 0)
-                prefetch_l2(p.q + ((size_t)s.b * p.rows + (size_t)tile * kTileRows) * kD, (uint32_t)rows * kD * 2);
-    }
-    auto hand_over = [&](uint32_t k) {
-        fence_proxy_async_smem();  // this lane's completed copies, before the MMA's reads
-        __syncwarp();
-        if (lane == 0) mbar_arrive(c.bar(B_KFULL + r * kRingSlots + (int)(k % kRingSlots)));
-    };
     walk.init(p, part);
     uint32_t issued = 0, step = 0;
     bool ok = true;
@@ -530,22 +543,22 @@ __device__ void score_producer_sparse(const DecodeParams &p, const Ctx &c, int p
         for (int pg = s.p0; ok && pg < s.p1; pg += 2, ++step) {
             const int npg = min(2, s.p1 - pg);
             if ((int)(step % kScoreIssuers) != r) continue;  // the other ring's step
-            const uint8_t *src[4];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-                src[q4] = (q4 < 2 || npg > 1) ? sparse_row(p, list, list_len, T, s.b, kPage * pg + 32 * q4 + lane)
-                                              : nullptr;
-            const uint32_t m0 = __ballot_sync(0xffffffffu, src[0] != nullptr),
-                           m1 = __ballot_sync(0xffffffffu, src[1] != nullptr),
-                           m2 = __ballot_sync(0xffffffffu, src[2] != nullptr),
-                           m3 = __ballot_sync(0xffffffffu, src[3] != nullptr);
+            int y[4];
+            const uint32_t v = sparse_rows(p, list, list_len, T, s.b, kPage * pg + 4 * lane, lane < 16 * npg, y);
+            const uint32_t b0 = __ballot_sync(0xffffffffu, v & 1u), b1 = __ballot_sync(0xffffffffu, v & 2u),
+                           b2 = __ballot_sync(0xffffffffu, v & 4u), b3 = __ballot_sync(0xffffffffu, v & 8u);
             const int sc = (int)(step % kScSlots);
             if (!warp_wait(c, B_SCEMPTY + sc, ((step / kScSlots) & 1) ^ 1)) {
                 ok = false;
                 break;
             }
             if (lane == 0) {
-                sts128(smem_u32(c.base + kScaleOff + sc * kScBytes), m0, m1, m2, m3);
+                // row 4 i + j of a page is bit i of ballot j
+                const uint64_t ma = spread4(b0) | spread4(b1) << 1 | spread4(b2) << 2 | spread4(b3) << 3;
+                const uint64_t mb = spread4(b0 >> 16) | spread4(b1 >> 16) << 1 | spread4(b2 >> 16) << 2 |
+                                    spread4(b3 >> 16) << 3;
+                sts128(smem_u32(c.base + kScaleOff + sc * kScBytes), (uint32_t)ma, (uint32_t)(ma >> 32), (uint32_t)mb,
+                       (uint32_t)(mb >> 32));
                 mbar_arrive(c.bar(B_SCFULL + sc));
             }
             for (int ch = 0; ch < kKChunks; ++ch) {
@@ -555,38 +568,29 @@ __device__ void score_producer_sparse(const DecodeParams &p, const Ctx &c, int p
                     ok = false;
                     break;
                 }
-                const uint32_t slot = smem_u32(c.base + kKRingOff + sl * kSlotBytes);
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    if (q4 >= 2 && npg < 2) break;
-                    const int R = 32 * q4 + lane;
-                    const uint32_t row = slot + 128u * (uint32_t)R;
-                    const uint8_t *g = src[q4] ? src[q4] + ch * 128 : reinterpret_cast<const uint8_t *>(p.kcache);
-                    const uint32_t nb = src[q4] ? 16u : 0u;
-#pragma unroll
-                    for (int cc = 0; cc < 8; ++cc)
-                        cp_async16(row + 16u * (uint32_t)(cc ^ (R & 7)), g + (src[q4] ? 16 * cc : 0), nb);
-                }
-                cp_async_commit();
+                if (lane == 0) mbar_arrive_expect_tx(c.bar(B_KFULL + sl), npg * kChunkBytes);
+                __syncwarp();
+                if (lane < 16 * npg)
+                    tma_gather4(smem_u32(c.base + kKRingOff + sl * kSlotBytes) + 512u * (uint32_t)lane, map,
+                                c.bar(B_KFULL + sl), 64 * ch, y[0], y[1], y[2], y[3]);
                 ++issued;
-                if (k >= (uint32_t)kGatherLag) {
-                    cp_async_wait<kGatherLag>();
-                    hand_over(k - kGatherLag);
-                }
             }
         }
     }
-    cp_async_wait<0>();  // no copy may be in flight when this CTA exits
-    if (ok)
-        for (uint32_t k = issued > (uint32_t)kGatherLag ? issued - kGatherLag : 0; k < issued; ++k) hand_over(k);
+    // the last gathers must have landed before this CTA may exit (already
+    // true on the normal path, where the MMAs consumed them)
+    if (lane == 0)
+        for (uint32_t k = issued > (uint32_t)kRingSlots ? issued - kRingSlots : 0; k < issued; ++k)
+            mbar_wait(c.bar(B_KFULL + r * kRingSlots + (int)(k % kRingSlots)), (k / kRingSlots) & 1, c.status);
     __syncwarp();
 }
 
-// Value-CTA producer of the sparse decode; the whole warp runs it.  Lane l
-// gathers rows l and l + 32 of each list chunk (dims 0..511: 8 chunks x 8
-// copies per row) into the V stage; a stage is handed over (B_VFULL) once its
-// copies are complete, one page later.
-__device__ void value_producer_sparse(const DecodeParams &p, const Ctx &c, int part, int tile) {
+// Value-CTA producer of the sparse decode; the whole warp runs it.  Lane i
+// (i < 16) gathers the page's rows 4 i .. 4 i + 3, dims 0..511 (one gather
+// per 64-dim chunk), into the V stage, whose barrier lane 0 has armed with
+// the stage's bytes.
+__device__ void value_producer_sparse(const DecodeParams &p, const Ctx &c, const CUtensorMap *map, int part,
+                                      int tile) {
     const int lane = threadIdx.x & 31;
     const int qtok = p.s_q == 1 ? 0 : tile;
     PartWalk walk;
@@ -594,45 +598,32 @@ __device__ void value_producer_sparse(const DecodeParams &p, const Ctx &c, int p
     walk.init(p, part);
     uint32_t it = 0;
     bool ok = true;
-    auto hand_over = [&](uint32_t k) {
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(c.bar(B_VFULL + (int)(k % kVStages)));
-    };
     while (ok && walk.next(p, s)) {
         const int T = sparse_cache_len(p, s.b);
         const int32_t *list = p.indices + ((size_t)s.b * p.s_q + qtok) * p.topk;
         const int list_len = min(s.T, p.topk);
         for (int pg = s.p0; pg < s.p1; ++pg, ++it) {
             const int st = it % kVStages;
+            int y[4];
+            sparse_rows(p, list, list_len, T, s.b, kPage * pg + 4 * lane, lane < 16, y);
             if (!warp_wait(c, B_VEMPTY + st, ((it / kVStages) & 1) ^ 1)) {
                 ok = false;
                 break;
             }
-            const uint32_t stage = smem_u32(c.base + kVRingOff + st * kVStageBytes);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int R = 32 * h + lane;
-                const uint8_t *src = sparse_row(p, list, list_len, T, s.b, kPage * pg + R);
-                const uint8_t *g = src ? src : reinterpret_cast<const uint8_t *>(p.kcache);
-                const uint32_t nb = src ? 16u : 0u;
+            if (lane == 0) mbar_arrive_expect_tx(c.bar(B_VFULL + st), kVStageBytes);
+            __syncwarp();
+            if (lane < 16) {
+                const uint32_t stage = smem_u32(c.base + kVRingOff + st * kVStageBytes) + 512u * (uint32_t)lane;
 #pragma unroll
                 for (int ch = 0; ch < kVChunks; ++ch)
-#pragma unroll
-                    for (int cc = 0; cc < 8; ++cc)
-                        cp_async16(stage + (uint32_t)ch * kChunkBytes + 128u * (uint32_t)R +
-                                       16u * (uint32_t)(cc ^ (R & 7)),
-                                   g + (src ? ch * 128 + 16 * cc : 0), nb);
-            }
-            cp_async_commit();
-            if (it > 0) {
-                cp_async_wait<1>();
-                hand_over(it - 1);
+                    tma_gather4(stage + (uint32_t)ch * kChunkBytes, map, c.bar(B_VFULL + st), 64 * ch, y[0], y[1], y[2],
+                                y[3]);
             }
         }
     }
-    cp_async_wait<0>();
-    if (ok && it > 0) hand_over(it - 1);
+    if (lane == 0)
+        for (uint32_t k = it > (uint32_t)kVStages ? it - kVStages : 0; k < it; ++k)
+            mbar_wait(c.bar(B_VFULL + (int)(k % kVStages)), (k / kVStages) & 1, c.status);
     __syncwarp();
 }
 
@@ -1265,9 +1256,9 @@ split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParam
         if (kFp8 && is_score) {
             score_producer_e4m3(p, c, &kv_map, part, tile, warp == 0 ? 0 : 1);
         } else if (kSparse && is_score) {
-            score_producer_sparse(p, c, part, tile, warp == 0 ? 0 : 1);
+            score_producer_sparse(p, c, &kv_map, part, tile, warp == 0 ? 0 : 1);
         } else if (kSparse) {
-            if (warp == 0) value_producer_sparse(p, c, part, tile);
+            if (warp == 0) value_producer_sparse(p, c, &kv_map, part, tile);
         } else if (elect_one_lane() && (warp == 0 || (is_score && kScoreIssuers > 1))) {
             if (is_score) score_producer(p, c, &kv_map, part, tile, warp == 0 ? 0 : 1);
             else value_producer(p, c, &kv_map, part);
@@ -1320,6 +1311,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 bool make_kv_map(CUtensorMap *m, const void *kcache, int64_t num_blocks) {
     auto enc = encode_fn();
     if (!enc) return false;
+    if constexpr (kSparse) {
+        // gathers: the cache as a 2-D tensor of num_blocks * 64 rows of D
+        // elements, one 64-element row per box (tile::gather4 takes 4 rows)
+        cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)num_blocks * kPage};
+        cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+        cuuint32_t box[2] = {64, 1};
+        cuuint32_t es[2] = {1, 1};
+        return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(kcache), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
     if constexpr (kFp8) {
         cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)kPage, (cuuint64_t)num_blocks};
         cuuint64_t strides[2] = {(cuuint64_t)kD, (cuuint64_t)kE4PageBytes};

@@ -228,6 +228,7 @@ def _decode_sparse(lib, **over):
     (dict(topk=0), _lib.MLA_ERR_INVALID_ARG),
     (dict(d=512), _lib.MLA_ERR_UNSUPPORTED),           # 576-wide rows only
     (dict(s_q=2, h_q=64), _lib.MLA_ERR_UNSUPPORTED),   # a row tile must hold one query token
+    (dict(num_blocks=1 << 25), _lib.MLA_ERR_UNSUPPORTED),  # gathered rows need 32-bit row coordinates
     (dict(ws_bytes=1024), _lib.MLA_ERR_WORKSPACE),
 ])
 def test_sparse_decode_rejects_bad_arguments_before_launch(lib, over, code):
