@@ -93,5 +93,32 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB_PATH
 
 
+# test-only library: the same objects, but the bf16 d = 576 split kernel built
+# with a 1 ms wait limit and part 0 skipping one chunk load, so that a bounded
+# wait runs out on purpose (never the product library)
+TIMEOUT_TEST_LIB = os.path.join(BUILD_DIR, "libmla_decode_gb300_timeout_test.so")
+TIMEOUT_TEST_DEFINES = ["-DMLA_WAIT_LIMIT_NS=1000000ull", "-DMLA_TEST_SKIP_ONE_LOAD"]
+
+
+def build_timeout_test_lib(force: bool = False) -> str:
+    """Build the test-only library for the bounded-wait timeout test; returns its path."""
+    build()
+    src = os.path.join(CSRC, "mla_split_tc.cu")
+    obj = os.path.join(BUILD_DIR, "mla_split_tc_timeout_test.o")
+    if force or _stale(obj, [src, *_headers()]):
+        cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *TIMEOUT_TEST_DEFINES, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on the timeout test object:\n{r.stderr[-4000:]}")
+    objs = [os.path.join(BUILD_DIR, os.path.splitext(os.path.basename(x))[0] + ".o") for x in _sources()
+            if os.path.basename(x) != "mla_split_tc.cu"] + [obj]
+    if force or _stale(TIMEOUT_TEST_LIB, objs):
+        cmd = [nvcc(), *ARCH, "-shared", "-Xcompiler", "-fPIC", *objs, "-o", TIMEOUT_TEST_LIB]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stderr[-4000:]}")
+    return TIMEOUT_TEST_LIB
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

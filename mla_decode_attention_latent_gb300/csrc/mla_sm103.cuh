@@ -93,7 +93,12 @@ __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any legitimate wait
+// 2 s: far beyond any legitimate wait.  A test build of the library may set a
+// shorter limit (MLA_WAIT_LIMIT_NS) to exercise the timeout path quickly.
+#ifndef MLA_WAIT_LIMIT_NS
+#define MLA_WAIT_LIMIT_NS 2000000000ull
+#endif
+constexpr uint64_t kWaitLimitNs = MLA_WAIT_LIMIT_NS;
 
 // Wait for the phase with the given parity to complete.  Returns false (and
 // raises MLA_DEVERR_TIMEOUT) if it does not complete within kWaitLimitNs.

@@ -347,6 +347,12 @@ __device__ void score_producer(const DecodeParams &p, const Ctx &c, const CUtens
                     ok = false;
                     break;
                 }
+#ifdef MLA_TEST_SKIP_ONE_LOAD
+                // test builds only: part 0 never loads its third chunk, so the
+                // slot's barrier never completes and the MMA issuer's bounded
+                // wait must run out (MLA_DEVERR_TIMEOUT) and unwind the pair
+                if (part == 0 && tile == 0 && r == 0 && k == 2) continue;
+#endif
                 uint8_t *dst = c.base + kKRingOff + sl * kSlotBytes;
                 mbar_arrive_expect_tx(c.bar(B_KFULL + sl), npg * kChunkBytes);
                 tma_load_3d(dst, map, c.bar(B_KFULL + sl), 64 * ch, 0, blk0);
