@@ -96,29 +96,40 @@ constexpr bool kRing = kFp8 || kSparse;          // a per-step side ring (e4m3: 
 constexpr int kThreads = 256;                  // 8 warps: TMA, MMA, 4 row warps, second score MMA issuer and TMA producer
 constexpr int kTileRows = 128;                 // query rows per tile = TMEM lanes
 constexpr int kScoreIssuers = 2;               // score-CTA MMA issuers (and TMA producers), alternating steps
-// score CTA: 16 KB MMA operand slots, one ring per issuer: 5 each for a bf16
-// cache; 2 each for an e4m3 cache, whose codes land in separate rings of
-// kLandSlots 8 KB buffers and are widened into these slots
+// Pages per score step: two for bf16 rows (one tcgen05 MMA with N = 128
+// covers both), one for e4m3 pages, whose scores are three fp8 contractions
+// (see below) and whose S buffers are therefore one page wide.
+constexpr int kStepPages = kFp8 ? 1 : 2;
+// score CTA: MMA operand slots, one ring per issuer: for bf16 rows 5 each of
+// 16 KB (one 64-dim chunk of two pages); for e4m3 pages 2 each of 36 KB (the
+// nine 64-code chunks of one page, each a 64-byte-swizzled [64 x 64 B] tile)
 constexpr int kKSlots = kFp8 ? 4 : 10;
 constexpr int kRingSlots = kKSlots / kScoreIssuers;  // slots per score-MMA issuer's ring
-constexpr int kLandSlots = 6;                        // e4m3: landing buffers per ring
 constexpr int kVStages = 2;                    // value CTA ring: whole pages (dims 0..511)
-constexpr int kSBufs = 2;                      // S buffers in TMEM (score CTA), one per step of two pages
+constexpr int kSBufs = 2;                      // S buffers in TMEM (score CTA), one per step
 constexpr int kPBufs = 2;                      // P buffers (staging in the score CTA, landing in the value CTA)
 constexpr int kKChunks = kD / 64;              // 9 (or 8) chunks of 64 dims (128 B rows)
 constexpr int kVChunks = kDv / 64;             // 8
 constexpr int kLatChunks = kDv / 64;           // 8 latent chunks: the Q part kept in TMEM
 constexpr uint32_t kChunkBytes = kPage * 128;  // 64 tokens x 128 B = 8 KB
-constexpr uint32_t kSlotBytes = 2 * kChunkBytes;          // 16 KB: one chunk of two pages (128 token rows)
+constexpr uint32_t kE4ChunkBytes = kPage * 64;             // one 64-code chunk of one e4m3 page: 4 KB
+constexpr uint32_t kSlotBytes = kFp8 ? kKChunks * kE4ChunkBytes : 2 * kChunkBytes;  // 36 KB / 16 KB
 constexpr uint32_t kVStageBytes = kVChunks * kChunkBytes;  // 64 KB
 constexpr uint32_t kPBytes = kTileRows * 128;             // 16 KB: 128 rows x 64 bf16, 128B-swizzled
 constexpr uint32_t kFacOff = kPBytes;                      // then fac[128] (fp32)
 constexpr uint32_t kInvLOff = kPBytes + kTileRows * 4;     // then inv_l[128] (fp32)
 constexpr uint32_t kPMsgBytes = kPBytes + 2 * kTileRows * 4;  // 17 KB, a multiple of 1 KB
-constexpr uint32_t kQCols = kDv / 2;                       // Q latent: 256 TMEM columns of bf16 pairs
+// e4m3 pages: q is split per row into three e4m3 parts, q / sigma_r ~ h + m + l
+// (sigma_r = max |q_r| / 448), each contracted with the codes in fp8 on the
+// tensor cores; the latent dims of the three parts sit in TMEM (four codes
+// per column), their RoPE dims in 64-byte-swizzled shared tiles
+constexpr int kQParts = kFp8 ? 3 : 1;
+constexpr uint32_t kQPartCols = kDv / 4;                   // e4m3: one part's 512 latent codes = 128 columns
+constexpr uint32_t kQCols = kFp8 ? kQParts * kQPartCols : kDv / 2;  // bf16: 256 columns of bf16 pairs
 constexpr uint32_t kSCol0 = kQCols;                        // S buffers follow Q
-constexpr uint32_t kSCols = 2 * kPage;                     // an S buffer holds the scores of two pages
+constexpr uint32_t kSCols = kStepPages * kPage;            // an S buffer holds the scores of one step
 constexpr uint32_t kTmemCols = 512;
+static_assert(kSCol0 + kSBufs * kSCols <= kTmemCols, "tensor memory of the score CTA");
 constexpr float kRescaleLog2 = 8.0f;                       // lazy rescale threshold (log2 units)
 constexpr uint32_t kEpiCols = 64;                          // epilogue chunk: 64 fp32 columns
 constexpr uint32_t kEpiStride = kEpiCols * 4 + 16;         // padded row stride (conflict-free v4 stores)
@@ -126,23 +137,23 @@ constexpr uint32_t kEpiStride = kEpiCols * 4 + 16;         // padded row stride 
 static_assert(!kFp8 || kD == kDqk, "the e4m3 cache holds 576-wide rows");
 constexpr uint32_t kE4PageBytes = kPage * kD + kPage * 4;  // 64 rows of codes, then 64 fp32 scales
 constexpr uint32_t kE4ScaleOff = kPage * kD;               // the scales' byte offset in a page
-constexpr uint32_t kE4ChunkBytes = kPage * 64;             // one 64-dim chunk of one page: 4 KB of codes
-constexpr uint32_t kLandBytes = 2 * kE4ChunkBytes;         // a landing buffer: one chunk of two pages (8 KB)
 constexpr uint32_t kVLandOff = kVStageBytes / 2;           // e4m3 page landing inside a V stage (upper 32 KB)
 constexpr float kE4ScaleLimit = 255.f;                     // |scale| bound: P (< 2^8) times it stays in f16 range
-constexpr int kScSlots = 8;                                // scale ring: one slot per step of two pages (a producer
-                                                           // waits on the rows of 8 steps back: never in practice)
-constexpr uint32_t kScBytes = 2 * kPage * 4;               // 512 B
+constexpr float kE4Max = 448.f;                            // largest finite e4m3 value
+constexpr int kScSlots = 8;                                // side ring: one slot per step (a producer waits on
+                                                           // the rows of 8 steps back: never in practice)
+constexpr uint32_t kScBytes = kStepPages * kPage * 4;      // e4m3: the step's token scales; sparse: key masks
 static_assert(kE4PageBytes % 16 == 0 && kE4ScaleOff % 16 == 0, "TMA and bulk-copy alignment of e4m3 pages");
 
 // shared-memory layout (offsets from the 1024-byte aligned base)
 // score CTA: [K operand rings 2 x 5 x 16 KB][Q RoPE tile 16 KB][P staging 2 x 17 KB];
-// e4m3: [operand rings 2 x 2 x 16 KB][landing rings 2 x 6 x 8 KB][Q RoPE][P staging][scales 8 x 512 B]
+// e4m3: [operand rings 2 x 2 x 36 KB][Q RoPE tiles 3 x 8 KB][P staging][scales 8 x 256 B];
+// sparse: [operand rings][Q RoPE][P staging][key masks 8 x 512 B]
 constexpr uint32_t kKRingOff = 0;
-constexpr uint32_t kLandOff = kKRingOff + kKSlots * kSlotBytes;  // e4m3: the landing rings
-constexpr uint32_t kQRopeOff = kLandOff + (kFp8 ? kScoreIssuers * kLandSlots * kLandBytes : 0);
-constexpr uint32_t kStageOff = kQRopeOff + (kHasRope ? kTileRows * 128 : 0);
-constexpr uint32_t kScaleOff = kStageOff + kPBufs * kPMsgBytes;   // e4m3: per-token scales of the steps in flight
+constexpr uint32_t kQRopeOff = kKRingOff + kKSlots * kSlotBytes;
+constexpr uint32_t kQRopePartBytes = kTileRows * (kFp8 ? 64 : 128);  // one part's [128 rows] RoPE tile
+constexpr uint32_t kStageOff = kQRopeOff + (kHasRope ? kQParts * kQRopePartBytes : 0);
+constexpr uint32_t kScaleOff = kStageOff + kPBufs * kPMsgBytes;   // the side ring of the steps in flight
 constexpr uint32_t kScoreEnd = kScaleOff + (kRing ? kScSlots * kScBytes : 0);
 // value CTA: [V ring 2 x 64 KB][P landing 2 x 17 KB][epilogue staging 34 KB]
 constexpr uint32_t kVRingOff = 0;
@@ -151,7 +162,8 @@ constexpr uint32_t kEpiOff = kPBufOff + kPBufs * kPMsgBytes;
 constexpr uint32_t kValueEnd = kEpiOff + kTileRows * kEpiStride;
 // barriers at the same offset in both CTAs (the peer arrives on some of them)
 constexpr uint32_t kBarOff = ((kScoreEnd > kValueEnd ? kScoreEnd : kValueEnd) + 1023u) & ~1023u;
-static_assert(kQRopeOff % 1024 == 0 && kStageOff % 1024 == 0 && kPBufOff % 1024 == 0 && kPMsgBytes % 1024 == 0,
+static_assert(kQRopeOff % 1024 == 0 && kStageOff % 1024 == 0 && kPBufOff % 1024 == 0 && kPMsgBytes % 1024 == 0 &&
+                  kSlotBytes % 1024 == 0,
               "swizzled tiles need 1 KB alignment");
 
 enum Bar {
@@ -164,10 +176,11 @@ enum Bar {
     // both
     B_FINAL = B_OEMPTY + 1, B_BASE_COUNT = B_FINAL + 1
 };
-// e4m3 cache only: landing of the codes (the converters then arrive on
-// B_KFULL / B_VFULL), and the scale ring of the score CTA
-constexpr int B_KLAND = B_BASE_COUNT, B_VLAND = B_KLAND + kScoreIssuers * kLandSlots, B_SCFULL = B_VLAND + kVStages,
-              B_SCEMPTY = B_SCFULL + kScSlots, B_VREAD = B_SCEMPTY + kScSlots;
+// e4m3 pages and sparse lists: landing of the value CTA's codes (its row warps
+// then widen them and arrive on B_VFULL), the score CTA's side ring, and the
+// value CTA's read-before-write barrier of the in-place widening
+constexpr int B_VLAND = B_BASE_COUNT, B_SCFULL = B_VLAND + kVStages, B_SCEMPTY = B_SCFULL + kScSlots,
+              B_VREAD = B_SCEMPTY + kScSlots;
 constexpr int B_COUNT = kRing ? B_VREAD + 1 : B_BASE_COUNT;
 constexpr uint32_t kTmemSlotOff = kBarOff + B_COUNT * 8;
 constexpr uint32_t kAbortOff = kTmemSlotOff + 4;
@@ -366,111 +379,53 @@ __device__ void score_producer(const DecodeParams &p, const Ctx &c, const CUtens
         mbar_wait(c.bar(B_KFULL + r * kRingSlots + (int)(k % kRingSlots)), (k / kRingSlots) & 1, c.status);
 }
 
-// Score-CTA producer for the e4m3 cache; the whole warp runs it.  Lane 0
-// issues each chunk's codes (4 KB per page) into the next buffer of this
-// ring's landing ring, completing on its B_KLAND, and each step's per-token
-// scales (one 256 B bulk copy per page) into the scale ring.  The warp widens
-// the chunks in order, each into the ring's next MMA operand slot once the MMA
-// has freed it (B_KEMPTY), and arrives on the slot's B_KFULL, which the MMA
-// issuer waits for as with a bf16 cache.  A landing buffer is reused as soon as
-// its chunk is widened, so up to kLandSlots chunks are in flight whatever the
-// MMA does.  Block ids come from a window of 32 table entries held one per lane.
-__device__ void score_producer_e4m3(const DecodeParams &p, const Ctx &c, const CUtensorMap *map, int part, int tile,
-                                   int r) {
-    const int lane = threadIdx.x & 31;
+// Score-CTA TMA producer for e4m3 pages (one lane per issuer's ring `r`,
+// taking the steps of parity r).  A step is one page: its slot receives the
+// page's nine 64-code chunks as 64-byte-swizzled [64 x 64 B] tiles, which the
+// fp8 MMAs read as they are, and the page's 64 per-token scales go to the side
+// ring (one 256 B bulk copy).
+__device__ void score_producer_e4m3(const DecodeParams &p, const Ctx &c, const CUtensorMap *map, int part, int r) {
     const uint8_t *kv = reinterpret_cast<const uint8_t *>(p.kcache);
     PartWalk walk;
     Segment s;
-    if (lane == 0 && r == 0) {
-        const int rows = min(kTileRows, p.rows - tile * kTileRows);
-        walk.init(p, part);
-        while (walk.next(p, s))
-            if (s.p1 > s.p0 && rows > 0)
-                prefetch_l2(p.q + ((size_t)s.b * p.rows + (size_t)tile * kTileRows) * kD, (uint32_t)rows * kD * 2);
-    }
-    int win_b = -1, win_pg = 0, win_blk = 0;  // lane i holds block_table[win_b][win_pg + i]
-    auto block_of = [&](int b, int pg) -> int {
-        if (b != win_b || pg < win_pg || pg >= win_pg + 32) {
-            win_b = b;
-            win_pg = pg;
-            win_blk = pg + lane < p.max_blocks ? p.block_table[(size_t)b * p.max_blocks + pg + lane] : 0;
-        }
-        int blk = __shfl_sync(0xffffffffu, win_blk, pg - win_pg);
-        if (blk < 0 || (int64_t)blk >= p.num_blocks) {
-            if (lane == 0) atomicOr(p.status, MLA_DEVERR_BLOCK_ID);
-            blk = 0;
-        }
-        return blk;
-    };
-    uint32_t issued = 0, widened = 0;  // chunks of this ring: loaded into the landing ring / widened for the MMA
-    uint32_t two_page = 0;             // bit k % 32: chunk k holds two pages
-    const uint32_t land0 = smem_u32(c.base + kLandOff) + (uint32_t)(r * kLandSlots) * kLandBytes;
-    auto widen_next = [&]() -> bool {
-        const uint32_t k = widened;
-        const int ls = r * kLandSlots + (int)(k % kLandSlots), sl = r * kRingSlots + (int)(k % kRingSlots);
-        if (!warp_wait(c, B_KLAND + ls, (k / kLandSlots) & 1)) return false;
-        if (!warp_wait(c, B_KEMPTY + sl, ((k / kRingSlots) & 1) ^ 1)) return false;
-        const uint32_t slot = smem_u32(c.base + kKRingOff + sl * kSlotBytes);
-        const uint32_t land = land0 + (k % kLandSlots) * kLandBytes;
-        auto sync = [] {
-            __syncwarp();
-            return true;
-        };
-        if ((two_page >> (k & 31)) & 1u) widen_e4m3<16, 32>(slot, land, lane, kPage, sync);
-        else widen_e4m3<8, 32>(slot, land, lane, kPage, sync);
-        // orders this lane's shared-memory writes before the MMA's reads and its
-        // reads of the landing buffer before the next load into it
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(c.bar(B_KFULL + sl));
-        ++widened;
-        return true;
-    };
     walk.init(p, part);
-    uint32_t step = 0;
+    uint32_t ring_it = 0, step = 0, own = 0;
     bool ok = true;
     while (ok && walk.next(p, s)) {
-        for (int pg = s.p0; ok && pg < s.p1; pg += 2, ++step) {
-            const int npg = min(2, s.p1 - pg);
+        for (int pg = s.p0; ok && pg < s.p1; ++pg, ++step) {
             if ((int)(step % kScoreIssuers) != r) continue;  // the other ring's step
-            const int blk0 = block_of(s.b, pg);
-            const int blk1 = npg > 1 ? block_of(s.b, pg + 1) : 0;
+            const int blk = safe_block(p, s.b, pg);
             const int sc = (int)(step % kScSlots);
-            if (!warp_wait(c, B_SCEMPTY + sc, ((step / kScSlots) & 1) ^ 1)) {
+            if (!wait(c, B_SCEMPTY + sc, ((step / kScSlots) & 1) ^ 1)) {
                 ok = false;
                 break;
             }
-            if (lane == 0) {
-                uint8_t *dst = c.base + kScaleOff + sc * kScBytes;
-                mbar_arrive_expect_tx(c.bar(B_SCFULL + sc), (uint32_t)npg * kPage * 4);
-                bulk_load(dst, kv + (size_t)blk0 * kE4PageBytes + kE4ScaleOff, kPage * 4, c.bar(B_SCFULL + sc));
-                if (npg > 1)
-                    bulk_load(dst + kPage * 4, kv + (size_t)blk1 * kE4PageBytes + kE4ScaleOff, kPage * 4,
-                              c.bar(B_SCFULL + sc));
+            mbar_arrive_expect_tx(c.bar(B_SCFULL + sc), kPage * 4);
+            bulk_load(c.base + kScaleOff + sc * kScBytes, kv + (size_t)blk * kE4PageBytes + kE4ScaleOff, kPage * 4,
+                      c.bar(B_SCFULL + sc));
+            ++own;
+            const uint32_t k = ring_it;
+            const int sl = r * kRingSlots + (int)(k % kRingSlots);
+            if (!wait(c, B_KEMPTY + sl, ((k / kRingSlots) & 1) ^ 1)) {
+                ok = false;
+                break;
             }
-            for (int ch = 0; ch < kKChunks; ++ch) {
-                // the landing buffer of chunk `issued` holds chunk issued - kLandSlots until it is widened
-                while (ok && widened + kLandSlots <= issued) ok = widen_next();
-                if (!ok) break;
-                const uint32_t k = issued;
-                const int ls = r * kLandSlots + (int)(k % kLandSlots);
-                two_page = npg > 1 ? (two_page | (1u << (k & 31))) : (two_page & ~(1u << (k & 31)));
-                if (lane == 0) {
-                    uint8_t *dst = c.base + kLandOff + (size_t)ls * kLandBytes;
-                    mbar_arrive_expect_tx(c.bar(B_KLAND + ls), (uint32_t)npg * kE4ChunkBytes);
-                    tma_load_3d(dst, map, c.bar(B_KLAND + ls), 64 * ch, 0, blk0);
-                    if (npg > 1) tma_load_3d(dst + kE4ChunkBytes, map, c.bar(B_KLAND + ls), 64 * ch, 0, blk1);
-                }
-                ++issued;
-            }
+            uint8_t *dst = c.base + kKRingOff + sl * kSlotBytes;
+            mbar_arrive_expect_tx(c.bar(B_KFULL + sl), kSlotBytes);
+            for (int ch = 0; ch < kKChunks; ++ch)
+                tma_load_3d(dst + ch * kE4ChunkBytes, map, c.bar(B_KFULL + sl), 64 * ch, 0, blk);
+            ++ring_it;
         }
     }
-    while (ok && widened < issued) ok = widen_next();
-    // after an early exit, the loads in flight must land before this CTA may exit
-    if (lane == 0)
-        for (uint32_t k = widened; k < issued; ++k)
-            mbar_wait(c.bar(B_KLAND + r * kLandSlots + (int)(k % kLandSlots)), (k / kLandSlots) & 1, c.status);
-    __syncwarp();
+    // the last loads must have landed before this CTA may exit (already true
+    // on the normal path, where the MMAs and the row warps consumed them)
+    for (uint32_t k = ring_it > (uint32_t)kRingSlots ? ring_it - kRingSlots : 0; k < ring_it; ++k)
+        mbar_wait(c.bar(B_KFULL + r * kRingSlots + (int)(k % kRingSlots)), (k / kRingSlots) & 1, c.status);
+    const uint32_t back = own < (uint32_t)(kScSlots / kScoreIssuers) ? own : (uint32_t)(kScSlots / kScoreIssuers);
+    for (uint32_t i = own - back; i < own; ++i) {
+        const uint32_t st = (uint32_t)kScoreIssuers * i + (uint32_t)r;  // this ring's steps: every other step
+        mbar_wait(c.bar(B_SCFULL + (int)(st % kScSlots)), (st / kScSlots) & 1, c.status);
+    }
 }
 
 // -------------------------------------------------------------- sparse top-k gathers
@@ -689,7 +644,7 @@ __device__ void score_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, in
     const uint32_t ring = smem_u32(c.base + kKRingOff);
     const uint64_t rope_desc = desc_sw128(smem_u32(c.base + kQRopeOff), 16, 1024);
     while (walk.next(p, s)) {
-        const int nsteps = (s.p1 - s.p0 + 1) / 2;
+        const int nsteps = (s.p1 - s.p0 + kStepPages - 1) / kStepPages;
         if (!wait(c, B_QFULL, seg & 1)) return;  // Q of this segment is in TMEM and smem
         tc_fence_after();
         mbar_arrive(c.bar(B_QACK));              // the row warps may load the next Q only after both issuers saw this one
@@ -699,11 +654,40 @@ __device__ void score_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, in
             if ((int)(st % kScoreIssuers) != lane) continue;
             const int sb = (int)(st % kSBufs);
             const uint32_t d = tmem + kSCol0 + sb * kSCols;
-            const int npg = min(2, s.p1 - (s.p0 + 2 * j));
+            const int npg = min(kStepPages, s.p1 - (s.p0 + kStepPages * j));
             const uint32_t idesc = npg == 2 ? idesc_op(kTileRows, 2 * kPage, false, false)
                                             : idesc_op(kTileRows, kPage, false, false);
             if (!wait(c, B_SEMPTY + sb, ((st / kSBufs) & 1) ^ 1)) return;
             tc_fence_after();  // the row warps' reads of this S buffer come first
+            if constexpr (kFp8) {
+                // one page: S = sum over Q's three e4m3 parts t and the nine
+                // 64-code chunks of (part t) x (codes)^T, two K = 32 MMAs per
+                // chunk and part; A from TMEM (latent) or the part's RoPE tile
+                const uint32_t sl = lane * kRingSlots + ring_it % kRingSlots;
+                if (!wait(c, B_KFULL + sl, (ring_it / kRingSlots) & 1)) return;
+                const uint32_t slot = ring + sl * kSlotBytes;
+                constexpr uint32_t id8 = idesc_e4m3(kTileRows, kPage);
+#pragma unroll 1
+                for (int ch = 0; ch < kKChunks; ++ch) {
+                    const uint32_t b = slot + ch * kE4ChunkBytes;
+#pragma unroll
+                    for (int t = 0; t < kQParts; ++t) {
+                        if (ch < kLatChunks) {
+                            const uint32_t a = tmem + t * kQPartCols + ch * 16;
+                            mma_ts_f8(d, a, desc_sw64(b), id8, (ch | t) ? 1u : 0u);
+                            mma_ts_f8(d, a + 8, desc_sw64(b + 32), id8, 1u);
+                        } else {
+                            const uint32_t ar = smem_u32(c.base + kQRopeOff) + t * kQRopePartBytes;
+                            mma_ss_f8(d, desc_sw64(ar), desc_sw64(b), id8, 1u);
+                            mma_ss_f8(d, desc_sw64(ar + 32), desc_sw64(b + 32), id8, 1u);
+                        }
+                    }
+                }
+                mma_commit(c.bar(B_KEMPTY + sl));
+                ++ring_it;
+                mma_commit(c.bar(B_SFULL + sb));
+                continue;
+            }
             for (int ch = 0; ch < kKChunks; ++ch, ++ring_it) {
                 const uint32_t sl = lane * kRingSlots + ring_it % kRingSlots;
                 // TMA data: the barrier's completion already orders it before
@@ -789,13 +773,103 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
         // consumed all its S buffers, the MMAs reading it are done)
         if (seg > 0 && !warp_wait(c, B_QACK, (seg - 1) & 1)) return;
         ++seg;
+        float qsig = 1.f;  // e4m3 pages: this row's Q scale (q ~ qsig * (h + m + l))
         if (s.p1 > s.p0) {
-            // Q row r: latent dims 0..511 into TMEM lane r (columns 0..255,
-            // bf16 pairs, or f16 pairs for the e4m3 cache), RoPE dims 512..575
-            // into row r of the swizzled smem tile.  Two rounds of loads: the
-            // RoPE chunk with latent chunks 0..3 (40 loads in flight), then
-            // chunks 4..7.
             const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q + ((size_t)s.b * p.rows + (row_ok ? gr : 0)) * kD);
+            if constexpr (kFp8) {
+                // Q row r as three e4m3 parts of q / qsig (qsig = max |q| / 448):
+                // h = e4m3(x), m = e4m3(x - h), l = e4m3(x - h - m); latent dims
+                // into TMEM lane r (part t at columns 128 t + dim / 4), RoPE dims
+                // into row r of part t's 64-byte-swizzled tile
+                float amax = 0.f;
+#pragma unroll 1
+                for (int j0 = 0; j0 < kD / 8; j0 += 24) {
+                    uint4 x[24];
+#pragma unroll
+                    for (int j = 0; j < 24; ++j) x[j] = row_ok ? __ldg(qrow + j0 + j) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                    for (int j = 0; j < 24; ++j) {
+                        const uint32_t w4[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            amax = max3f(amax, fabsf(__uint_as_float(w4[e] << 16)),
+                                         fabsf(__uint_as_float(w4[e] & 0xffff0000u)));
+                    }
+                }
+                qsig = amax > 0.f ? amax / kE4Max : 1.f;
+                const float inv = 1.f / qsig;
+                // one 64-dim chunk: three parts of 16 words (four codes each)
+                auto split = [&](const uint4 (&x)[8], uint32_t (&ph)[16], uint32_t (&pm)[16], uint32_t (&pl)[16]) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t w4[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
+#pragma unroll
+                        for (int hw = 0; hw < 2; ++hw) {
+                            float v[4];
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                v[2 * e] = __uint_as_float(w4[2 * hw + e] << 16) * inv;
+                                v[2 * e + 1] = __uint_as_float(w4[2 * hw + e] & 0xffff0000u) * inv;
+                            }
+                            uint32_t code[3];
+#pragma unroll
+                            for (int t = 0; t < 3; ++t) {
+                                const uint32_t c01 = pack_e4m3x2(v[0], v[1]), c23 = pack_e4m3x2(v[2], v[3]);
+                                code[t] = c01 | (c23 << 16);
+                                if (t < 2) {
+                                    float d0, d1, d2, d3;
+                                    f16x2_to_f32(e4m3x2_to_f16x2(c01), d0, d1);
+                                    f16x2_to_f32(e4m3x2_to_f16x2(c23), d2, d3);
+                                    v[0] -= d0;
+                                    v[1] -= d1;
+                                    v[2] -= d2;
+                                    v[3] -= d3;
+                                }
+                            }
+                            ph[2 * j + hw] = code[0];
+                            pm[2 * j + hw] = code[1];
+                            pl[2 * j + hw] = code[2];
+                        }
+                    }
+                };
+#pragma unroll 1
+                for (int ch = 0; ch < kKChunks; ++ch) {
+                    // three chunks' loads per round (the first pass brought the row into L1)
+                    uint4 x[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) x[j] = row_ok ? __ldg(qrow + ch * 8 + j) : make_uint4(0, 0, 0, 0);
+                    if (ch % 3 == 0 && ch + 2 < kKChunks && row_ok) {
+                        prefetch_line_l1(qrow + (ch + 1) * 8);
+                        prefetch_line_l1(qrow + (ch + 1) * 8 + 4);
+                        prefetch_line_l1(qrow + (ch + 2) * 8);
+                        prefetch_line_l1(qrow + (ch + 2) * 8 + 4);
+                    }
+                    uint32_t ph[16], pm[16], pl[16];
+                    split(x, ph, pm, pl);
+                    if (ch < kLatChunks) {
+                        tmem_st16(tmem + lane_base + 0 * kQPartCols + ch * 16, ph);
+                        tmem_st16(tmem + lane_base + 1 * kQPartCols + ch * 16, pm);
+                        tmem_st16(tmem + lane_base + 2 * kQPartCols + ch * 16, pl);
+                    } else {
+                        // 64 B per row; 16-byte piece q of row r at q ^ ((r >> 1) & 3)
+                        const uint32_t rope = smem_u32(c.base + kQRopeOff) + (uint32_t)r * 64u;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint32_t off = 16u * (uint32_t)(q ^ ((r >> 1) & 3));
+                            sts128(rope + off, ph[4 * q], ph[4 * q + 1], ph[4 * q + 2], ph[4 * q + 3]);
+                            sts128(rope + kQRopePartBytes + off, pm[4 * q], pm[4 * q + 1], pm[4 * q + 2], pm[4 * q + 3]);
+                            sts128(rope + 2 * kQRopePartBytes + off, pl[4 * q], pl[4 * q + 1], pl[4 * q + 2],
+                                   pl[4 * q + 3]);
+                        }
+                        fence_proxy_async_smem();
+                    }
+                }
+                tmem_wait_st();
+            } else {
+            // Q row r: latent dims 0..511 into TMEM lane r (columns 0..255,
+            // bf16 pairs), RoPE dims 512..575 into row r of the swizzled smem
+            // tile.  Two rounds of loads: the RoPE chunk with latent chunks
+            // 0..3 (40 loads in flight), then chunks 4..7.
             uint4 y[kHasRope ? 8 : 1];
             if constexpr (kHasRope) {
 #pragma unroll
@@ -809,13 +883,8 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
                 if (kHasRope && ch0 == 0) {
                     const uint32_t rope = smem_u32(c.base + kQRopeOff) + (uint32_t)r * 128u;
 #pragma unroll
-                    for (int j = 0; j < (kHasRope ? 8 : 0); ++j) {
-                        uint4 v = y[j];
-                        if constexpr (kFp8)
-                            v = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
-                                           bf16x2_to_f16x2(v.w));
-                        sts128(rope + 16u * (uint32_t)(j ^ (r & 7)), v.x, v.y, v.z, v.w);
-                    }
+                    for (int j = 0; j < (kHasRope ? 8 : 0); ++j)
+                        sts128(rope + 16u * (uint32_t)(j ^ (r & 7)), y[j].x, y[j].y, y[j].z, y[j].w);
                     fence_proxy_async_smem();
                 }
 #pragma unroll
@@ -828,14 +897,11 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
                         v[4 * j + 2] = x[8 * k + j].z;
                         v[4 * j + 3] = x[8 * k + j].w;
                     }
-                    if constexpr (kFp8) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = bf16x2_to_f16x2(v[j]);
-                    }
                     tmem_st32(tmem + lane_base + (ch0 + k) * 32, v);
                 }
             }
             tmem_wait_st();
+            }
         }
         tc_fence_before();
         mbar_arrive(c.bar(B_QFULL));
@@ -843,7 +909,7 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
         float m = -CUDART_INF_F, l = 0.f;
         for (int pg = s.p0; pg < s.p1; ++pg, ++it) {
             const int pb = it % kPBufs;
-            const int q2 = (pg - s.p0) & 1;          // position of this page in its step
+            const int q2 = (pg - s.p0) % kStepPages;  // position of this page in its step
             const int sb = step % kSBufs;
             const int scs = (int)(step % kScSlots);  // e4m3: this step's slot in the scale ring
             if (q2 == 0 && !warp_wait(c, B_SFULL + sb, (step / kSBufs) & 1)) return;
@@ -897,7 +963,7 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
                 }
             }
             tmem_wait_ld();
-            if (q2 == 1 || pg == s.p1 - 1) {         // last page of the step: release its S buffer
+            if (q2 == kStepPages - 1 || pg == s.p1 - 1) {  // last page of the step: release its S buffer
                 tc_fence_before();
                 mbar_arrive(c.bar(B_SEMPTY + sb));
                 if constexpr (kRing) mbar_arrive(c.bar(B_SCEMPTY + scs));  // the scales / masks are in registers
@@ -916,7 +982,7 @@ __device__ void score_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
                     sr[2 * j + 1] = __float_as_uint(xb);
                 }
             }
-            const float sc = p.scale_log2;
+            const float sc = p.scale_log2 * qsig;  // e4m3 pages: the row's Q scale folded in
             // page maximum of scale * log2(e) * s over the visible keys, four
             // independent chains to keep the dependency depth short.  A full
             // page with a positive scale takes the maximum of the raw scores
@@ -1180,7 +1246,8 @@ __device__ void value_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
 
 // -------------------------------------------------------------- kernel
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p) {
+split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap kv_map2,
+                   const DecodeParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t rank = cluster_ctarank();
@@ -1213,7 +1280,6 @@ split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParam
             }
         }
         if constexpr (kFp8) {
-            for (int i = 0; i < kScoreIssuers * kLandSlots; ++i) mbar_init(c.bar(B_KLAND + i), 1);
             for (int i = 0; i < kVStages; ++i) mbar_init(c.bar(B_VLAND + i), 1);
             for (int i = 0; i < kScSlots; ++i) {
                 mbar_init(c.bar(B_SCFULL + i), 1);
@@ -1239,6 +1305,7 @@ split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParam
         *c.abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&kv_map);
+        if constexpr (kFp8) tma_prefetch_desc(&kv_map2);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
@@ -1260,14 +1327,14 @@ split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParam
 
     if (warp == 0 || warp == 7) {
         if (kFp8 && is_score) {
-            score_producer_e4m3(p, c, &kv_map, part, tile, warp == 0 ? 0 : 1);
+            if (elect_one_lane()) score_producer_e4m3(p, c, &kv_map, part, warp == 0 ? 0 : 1);
         } else if (kSparse && is_score) {
             score_producer_sparse(p, c, &kv_map, part, tile, warp == 0 ? 0 : 1);
         } else if (kSparse) {
             if (warp == 0) value_producer_sparse(p, c, &kv_map, part, tile);
         } else if (elect_one_lane() && (warp == 0 || (is_score && kScoreIssuers > 1))) {
             if (is_score) score_producer(p, c, &kv_map, part, tile, warp == 0 ? 0 : 1);
-            else value_producer(p, c, &kv_map, part);
+            else value_producer(p, c, kFp8 ? &kv_map2 : &kv_map, part);
         }
     } else if (warp == 1 || warp == 6) {
         if (elect_one_lane() && (warp == 1 || (is_score && kScoreIssuers > 1))) {
@@ -1314,7 +1381,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // the tcgen05 K-major (K) and MN-major (V) operand descriptors expect.
 // e4m3 pages: the codes of a page viewed as {D bytes, 64, num_blocks} with the
 // page stride; a box (64 codes x 64 tokens) lands unswizzled, 64 B per token.
-bool make_kv_map(CUtensorMap *m, const void *kcache, int64_t num_blocks) {
+// The tensor maps of the cache.  bf16 rows: `m` only.  e4m3 pages: `m` lands
+// each 64-code box with the 64-byte swizzle of the fp8 MMA operands (score
+// CTA), `m2` unswizzled, 64 B per token, for the value CTA's widening.
+bool make_kv_map(CUtensorMap *m, CUtensorMap *m2, const void *kcache, int64_t num_blocks) {
     auto enc = encode_fn();
     if (!enc) return false;
     if constexpr (kSparse) {
@@ -1334,9 +1404,13 @@ bool make_kv_map(CUtensorMap *m, const void *kcache, int64_t num_blocks) {
         cuuint32_t box[3] = {64, (cuuint32_t)kPage, 1};
         cuuint32_t es[3] = {1, 1, 1};
         return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(kcache), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
+               enc(m2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(kcache), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     }
+    *m2 = *m;
     cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)kPage, (cuuint64_t)num_blocks};
     cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)kPage * kD * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)kPage, 1};
@@ -1405,7 +1479,8 @@ cudaError_t launch_split_kv_tc<kD, kFp8>(const DecodeParams &p, cudaStream_t str
     if (e != cudaSuccess) return e;
     if ((e = prepare(dev)) != cudaSuccess) return e;
     CUtensorMap map;
-    if (!make_kv_map(&map, p.kcache, p.num_blocks)) return cudaErrorInvalidValue;
+    CUtensorMap map2;
+    if (!make_kv_map(&map, &map2, p.kcache, p.num_blocks)) return cudaErrorInvalidValue;
     const int tiles = (p.rows + kTileRows - 1) / kTileRows;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * p.num_parts, tiles, 1);
@@ -1417,7 +1492,7 @@ cudaError_t launch_split_kv_tc<kD, kFp8>(const DecodeParams &p, cudaStream_t str
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, split_kv_tc_kernel, map, p);
+    return cudaLaunchKernelEx(&cfg, split_kv_tc_kernel, map, map2, p);
 }
 
 }  // namespace mla
