@@ -52,14 +52,15 @@
 //
 // e4m3 cache (MLA_SPLIT_FP8 = 1, D = 576): a page holds 64 rows of e4m3 codes
 // followed by 64 fp32 per-token scales, and row j dequantizes to c_j * code_j
-// (include/mla_decode.h).  The codes are widened to f16 (exact for every e4m3
-// value) in shared memory: in the score CTA by the whole warp of each TMA
-// producer, from a ring of landing buffers into the MMA operand slots; in the
-// value CTA by its row warps, in place in the upper half of each V stage, also
-// zeroing the rows past a sequence's end.  Both MMAs then run in f16 (Q and P
-// rounded to f16).  A token's scale multiplies its score column before the
-// softmax and its P column before P V, so the accumulators see c_j * code_j
-// exactly as the dequantized row.
+// (include/mla_decode.h).  Scores run on the fp8 tensor cores: each q row is
+// split into three e4m3 parts (q / sigma_r ~ h + m + l, sigma_r = max |q_r| /
+// 448), and every part is contracted with the codes as they land (nine
+// 64-byte-swizzled chunks per page); the row warps sum the three and multiply
+// by sigma_r, the softmax scale and the token's scale.  The value CTA widens
+// its page's value codes to f16 (exact for every e4m3 value) in place in the
+// upper half of each V stage, zeroing the rows past a sequence's end, and runs
+// P V in f16 with P multiplied by the token's scale, so the accumulators see
+// c_j * code_j as the dequantized row.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
