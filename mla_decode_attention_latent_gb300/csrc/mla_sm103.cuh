@@ -168,6 +168,19 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// the same gather, written to the same shared-memory offset of every CTA in
+// `cta_mask` (this cluster's ranks) and completing the bytes on the barrier at
+// the same offset in each of them
+__device__ __forceinline__ void tma_gather4_multicast(uint32_t dst, const CUtensorMap *map, uint64_t *bar, int x,
+                                                      int y0, int y1, int y2, int y3, uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes.multicast::cluster "
+        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
 // bulk copy of `bytes` from this CTA's shared memory into a peer CTA's shared
 // memory; completes the transaction bytes on the peer's barrier
 __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const void *src, uint32_t bytes,

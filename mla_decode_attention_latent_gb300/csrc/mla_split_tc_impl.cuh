@@ -99,12 +99,17 @@ constexpr int kTileRows = 128;                 // query rows per tile = TMEM lan
 constexpr int kScoreIssuers = 2;               // score-CTA MMA issuers (and TMA producers), alternating steps
 // Pages per score step: two for bf16 rows (one tcgen05 MMA with N = 128
 // covers both), one for e4m3 pages, whose scores are three fp8 contractions
-// (see below) and whose S buffers are therefore one page wide.
-constexpr int kStepPages = kFp8 ? 1 : 2;
+// (see below) and whose S buffers are therefore one page wide, and one for
+// sparse lists, whose gathered pages both CTAs share (below).
+constexpr int kStepPages = (kFp8 || kSparse) ? 1 : 2;
 // score CTA: MMA operand slots, one ring per issuer: for bf16 rows 5 each of
 // 16 KB (one 64-dim chunk of two pages); for e4m3 pages 2 each of 36 KB (the
-// nine 64-code chunks of one page, each a 64-byte-swizzled [64 x 64 B] tile)
-constexpr int kKSlots = kFp8 ? 4 : 10;
+// nine 64-code chunks of one page, each a 64-byte-swizzled [64 x 64 B] tile).
+// Sparse lists use no ring: both CTAs hold the same two page buffers (all nine
+// 64-dim chunks of a gathered page, 72 KB each) at the same offsets, filled by
+// gathers that each CTA issues for part of the chunks and multicasts to both,
+// so that each SM's gather engine moves about half of a page's rows.
+constexpr int kKSlots = kFp8 ? 4 : (kSparse ? 2 : 10);
 constexpr int kRingSlots = kKSlots / kScoreIssuers;  // slots per score-MMA issuer's ring
 constexpr int kVStages = 2;                    // value CTA ring: whole pages (dims 0..511)
 constexpr int kSBufs = 2;                      // S buffers in TMEM (score CTA), one per step
@@ -115,7 +120,7 @@ constexpr int kLatChunks = kDv / 64;           // 8 latent chunks: the Q part ke
 constexpr uint32_t kChunkBytes = kPage * 128;  // 64 tokens x 128 B = 8 KB
 constexpr uint32_t kE4ChunkBytes = kPage * 64;             // one 64-code chunk of one e4m3 page: 4 KB
 constexpr uint32_t kSlotBytes = kFp8 ? kKChunks * kE4ChunkBytes : 2 * kChunkBytes;  // 36 KB / 16 KB
-constexpr uint32_t kVStageBytes = kVChunks * kChunkBytes;  // 64 KB
+constexpr uint32_t kVStageBytes = (kSparse ? kKChunks : kVChunks) * kChunkBytes;  // 64 KB (sparse: 72 KB page buffers)
 constexpr uint32_t kPBytes = kTileRows * 128;             // 16 KB: 128 rows x 64 bf16, 128B-swizzled
 constexpr uint32_t kFacOff = kPBytes;                      // then fac[128] (fp32)
 constexpr uint32_t kInvLOff = kPBytes + kTileRows * 4;     // then inv_l[128] (fp32)
@@ -149,14 +154,14 @@ static_assert(kE4PageBytes % 16 == 0 && kE4ScaleOff % 16 == 0, "TMA and bulk-cop
 // shared-memory layout (offsets from the 1024-byte aligned base)
 // score CTA: [K operand rings 2 x 5 x 16 KB][Q RoPE tile 16 KB][P staging 2 x 17 KB];
 // e4m3: [operand rings 2 x 2 x 36 KB][Q RoPE tiles 3 x 8 KB][P staging][scales 8 x 256 B];
-// sparse: [operand rings][Q RoPE][P staging][key masks 8 x 512 B]
+// sparse: [page buffers 2 x 72 KB][Q RoPE][P staging][key masks 8 x 256 B]
 constexpr uint32_t kKRingOff = 0;
-constexpr uint32_t kQRopeOff = kKRingOff + kKSlots * kSlotBytes;
+constexpr uint32_t kQRopeOff = kKRingOff + (kSparse ? kVStages * kVStageBytes : kKSlots * kSlotBytes);
 constexpr uint32_t kQRopePartBytes = kTileRows * (kFp8 ? 64 : 128);  // one part's [128 rows] RoPE tile
 constexpr uint32_t kStageOff = kQRopeOff + (kHasRope ? kQParts * kQRopePartBytes : 0);
 constexpr uint32_t kScaleOff = kStageOff + kPBufs * kPMsgBytes;   // the side ring of the steps in flight
 constexpr uint32_t kScoreEnd = kScaleOff + (kRing ? kScSlots * kScBytes : 0);
-// value CTA: [V ring 2 x 64 KB][P landing 2 x 17 KB][epilogue staging 34 KB]
+// value CTA: [V ring 2 x 64 KB (sparse: the page buffers)][P landing 2 x 17 KB][epilogue staging 34 KB]
 constexpr uint32_t kVRingOff = 0;
 constexpr uint32_t kPBufOff = kVRingOff + kVStages * kVStageBytes;
 constexpr uint32_t kEpiOff = kPBufOff + kPBufs * kPMsgBytes;
@@ -480,77 +485,86 @@ __device__ __forceinline__ uint64_t spread4(uint32_t x) {
     return v;
 }
 
-// Score-CTA producer of the sparse decode; the whole warp runs it.  The
-// step's 128 operand rows are list entries 64 pg .. 64 pg + 127; lane i
-// resolves entries 4 i .. 4 i + 3 (lanes 0..15 only for a one-page step) and
-// issues their gather for each 64-dim chunk into the chunk's ring slot, lane 0
-// having armed the slot's barrier with the chunk's bytes.  The validity masks
-// of the step's two list chunks go to the side ring for the row warps.  (The
-// gathers run at the TMA engine's rate for 128-byte row pieces, about
-// 10 GB/s per SM on GB300, which bounds this decode; looking the rows up
-// further ahead, or asking L2 for whole rows first, measured no faster.)
-__device__ void score_producer_sparse(const DecodeParams &p, const Ctx &c, const CUtensorMap *map, int part, int tile,
-                                      int r) {
+// Sparse decode: the gathers of a page are split between the two CTAs of the
+// pair.  Both CTAs resolve the page's list entries to cache rows (lane i < 16:
+// entries 4 i .. 4 i + 3) and gather four rows per lane and 64-dim chunk into
+// page buffer it % 2: the score CTA chunks 0..2 and rows 0..31 of chunk 3,
+// multicast to both CTAs, and the RoPE chunk 8 into its own buffer only; the
+// value CTA rows 32..63 of chunk 3 and chunks 4..7, multicast to both (4.5
+// chunks each).  Each CTA's barrier of the buffer expects the bytes that
+// land in that CTA (72 KB, 64 KB); a peer's bytes may complete on it before
+// the CTA has armed it, which the barrier's transaction count allows.  A
+// buffer is refilled only after the value CTA's P V of the page two earlier,
+// which follows the score CTA's MMAs of that page: the value producer waits
+// for it on its own barrier, the score producer on the P-free barrier that
+// the same MMA commit arrives on.
+constexpr int kSparseSplitChunk = 3;   // chunks below: the score CTA's; above: the value CTA's; this one by halves
+constexpr uint16_t kPairMask = 0x3;    // both CTAs of the cluster
+
+// Score-CTA producer of the sparse decode (the whole warp).  The validity mask
+// of each page's list chunk goes to the side ring for the row warps.  (The
+// gathers run at the TMA engine's rate for 128-byte row pieces, about 10 GB/s
+// per SM on GB300, which bounds this decode.)
+__device__ void score_producer_sparse(const DecodeParams &p, const Ctx &c, const CUtensorMap *map, int part,
+                                      int tile) {
     const int lane = threadIdx.x & 31;
     const int qtok = p.s_q == 1 ? 0 : tile;  // the tile's query token (h_q = 128 when s_q > 1)
     PartWalk walk;
     Segment s;
     walk.init(p, part);
-    uint32_t issued = 0, step = 0;
+    uint32_t it = 0;
     bool ok = true;
     while (ok && walk.next(p, s)) {
         const int T = sparse_cache_len(p, s.b);
         const int32_t *list = p.indices + ((size_t)s.b * p.s_q + qtok) * p.topk;
         const int list_len = min(s.T, p.topk);
-        for (int pg = s.p0; ok && pg < s.p1; pg += 2, ++step) {
-            const int npg = min(2, s.p1 - pg);
-            if ((int)(step % kScoreIssuers) != r) continue;  // the other ring's step
+        for (int pg = s.p0; ok && pg < s.p1; ++pg, ++it) {
+            const int b = (int)(it % kVStages);
             int y[4];
-            const uint32_t v = sparse_rows(p, list, list_len, T, s.b, kPage * pg + 4 * lane, lane < 16 * npg, y);
+            const uint32_t v = sparse_rows(p, list, list_len, T, s.b, kPage * pg + 4 * lane, lane < 16, y);
             const uint32_t b0 = __ballot_sync(0xffffffffu, v & 1u), b1 = __ballot_sync(0xffffffffu, v & 2u),
                            b2 = __ballot_sync(0xffffffffu, v & 4u), b3 = __ballot_sync(0xffffffffu, v & 8u);
-            const int sc = (int)(step % kScSlots);
-            if (!warp_wait(c, B_SCEMPTY + sc, ((step / kScSlots) & 1) ^ 1)) {
+            const int sc = (int)(it % kScSlots);
+            if (!warp_wait(c, B_SCEMPTY + sc, ((it / kScSlots) & 1) ^ 1)) {
                 ok = false;
                 break;
             }
             if (lane == 0) {
-                // row 4 i + j of a page is bit i of ballot j
+                // row 4 i + j of the page is bit i of ballot j
                 const uint64_t ma = spread4(b0) | spread4(b1) << 1 | spread4(b2) << 2 | spread4(b3) << 3;
-                const uint64_t mb = spread4(b0 >> 16) | spread4(b1 >> 16) << 1 | spread4(b2 >> 16) << 2 |
-                                    spread4(b3 >> 16) << 3;
-                sts128(smem_u32(c.base + kScaleOff + sc * kScBytes), (uint32_t)ma, (uint32_t)(ma >> 32), (uint32_t)mb,
-                       (uint32_t)(mb >> 32));
+                sts128(smem_u32(c.base + kScaleOff + sc * kScBytes), (uint32_t)ma, (uint32_t)(ma >> 32), 0u, 0u);
                 mbar_arrive(c.bar(B_SCFULL + sc));
             }
-            for (int ch = 0; ch < kKChunks; ++ch) {
-                const uint32_t k = issued;
-                const int sl = r * kRingSlots + (int)(k % kRingSlots);
-                if (!warp_wait(c, B_KEMPTY + sl, ((k / kRingSlots) & 1) ^ 1)) {
-                    ok = false;
-                    break;
-                }
-                if (lane == 0) mbar_arrive_expect_tx(c.bar(B_KFULL + sl), npg * kChunkBytes);
-                __syncwarp();
-                if (lane < 16 * npg)
-                    tma_gather4(smem_u32(c.base + kKRingOff + sl * kSlotBytes) + 512u * (uint32_t)lane, map,
-                                c.bar(B_KFULL + sl), 64 * ch, y[0], y[1], y[2], y[3]);
-                ++issued;
+            // page buffer b is free in both CTAs once the P V of page it - 2 is done
+            if (!warp_wait<true>(c, B_PFREE + b, ((it / kPBufs) & 1) ^ 1)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) mbar_arrive_expect_tx(c.bar(B_VFULL + b), kKChunks * kChunkBytes);
+            __syncwarp();
+            if (lane < 16) {
+                const uint32_t buf = smem_u32(c.base + kKRingOff + b * kVStageBytes) + 512u * (uint32_t)lane;
+                tma_gather4(buf + (uint32_t)kLatChunks * kChunkBytes, map, c.bar(B_VFULL + b), 64 * kLatChunks, y[0],
+                            y[1], y[2], y[3]);
+#pragma unroll
+                for (int ch = 0; ch <= kSparseSplitChunk; ++ch)
+                    if (ch < kSparseSplitChunk || lane < 8)
+                        tma_gather4_multicast(buf + (uint32_t)ch * kChunkBytes, map, c.bar(B_VFULL + b), 64 * ch, y[0],
+                                              y[1], y[2], y[3], kPairMask);
             }
         }
     }
-    // the last gathers must have landed before this CTA may exit (already
-    // true on the normal path, where the MMAs consumed them)
+    // the last pages' bytes (ours and the peer's) must have landed before
+    // this CTA may exit (already true on the normal path, where the MMAs
+    // waited for them)
     if (lane == 0)
-        for (uint32_t k = issued > (uint32_t)kRingSlots ? issued - kRingSlots : 0; k < issued; ++k)
-            mbar_wait(c.bar(B_KFULL + r * kRingSlots + (int)(k % kRingSlots)), (k / kRingSlots) & 1, c.status);
+        for (uint32_t k = it > (uint32_t)kVStages ? it - kVStages : 0; k < it; ++k)
+            mbar_wait(c.bar(B_VFULL + (int)(k % kVStages)), (k / kVStages) & 1, c.status);
     __syncwarp();
 }
 
-// Value-CTA producer of the sparse decode; the whole warp runs it.  Lane i
-// (i < 16) gathers the page's rows 4 i .. 4 i + 3, dims 0..511 (one gather
-// per 64-dim chunk), into the V stage, whose barrier lane 0 has armed with
-// the stage's bytes.
+// Value-CTA producer of the sparse decode (the whole warp): rows 32..63 of
+// chunk 3 and chunks 4..7 of each page, multicast to both CTAs.
 __device__ void value_producer_sparse(const DecodeParams &p, const Ctx &c, const CUtensorMap *map, int part,
                                       int tile) {
     const int lane = threadIdx.x & 31;
@@ -565,21 +579,22 @@ __device__ void value_producer_sparse(const DecodeParams &p, const Ctx &c, const
         const int32_t *list = p.indices + ((size_t)s.b * p.s_q + qtok) * p.topk;
         const int list_len = min(s.T, p.topk);
         for (int pg = s.p0; pg < s.p1; ++pg, ++it) {
-            const int st = it % kVStages;
+            const int b = (int)(it % kVStages);
             int y[4];
             sparse_rows(p, list, list_len, T, s.b, kPage * pg + 4 * lane, lane < 16, y);
-            if (!warp_wait(c, B_VEMPTY + st, ((it / kVStages) & 1) ^ 1)) {
+            if (!warp_wait(c, B_VEMPTY + b, ((it / kVStages) & 1) ^ 1)) {
                 ok = false;
                 break;
             }
-            if (lane == 0) mbar_arrive_expect_tx(c.bar(B_VFULL + st), kVStageBytes);
+            if (lane == 0) mbar_arrive_expect_tx(c.bar(B_VFULL + b), kVChunks * kChunkBytes);
             __syncwarp();
             if (lane < 16) {
-                const uint32_t stage = smem_u32(c.base + kVRingOff + st * kVStageBytes) + 512u * (uint32_t)lane;
+                const uint32_t buf = smem_u32(c.base + kVRingOff + b * kVStageBytes) + 512u * (uint32_t)lane;
 #pragma unroll
-                for (int ch = 0; ch < kVChunks; ++ch)
-                    tma_gather4(stage + (uint32_t)ch * kChunkBytes, map, c.bar(B_VFULL + st), 64 * ch, y[0], y[1], y[2],
-                                y[3]);
+                for (int ch = kSparseSplitChunk; ch < kVChunks; ++ch)
+                    if (ch > kSparseSplitChunk || lane >= 8)
+                        tma_gather4_multicast(buf + (uint32_t)ch * kChunkBytes, map, c.bar(B_VFULL + b), 64 * ch, y[0],
+                                              y[1], y[2], y[3], kPairMask);
             }
         }
     }
@@ -686,6 +701,29 @@ __device__ void score_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, in
                 }
                 mma_commit(c.bar(B_KEMPTY + sl));
                 ++ring_it;
+                mma_commit(c.bar(B_SFULL + sb));
+                continue;
+            }
+            if constexpr (kSparse) {
+                // one page from page buffer st % 2, all nine chunks at once
+                const int pb = (int)(st % kVStages);
+                if (!wait(c, B_VFULL + pb, (st / kVStages) & 1)) return;
+                const uint32_t buf = ring + pb * kVStageBytes;
+                for (int ch = 0; ch < kKChunks; ++ch) {
+                    const uint64_t bd = desc_sw128(buf + ch * kChunkBytes, 16, 1024);
+                    if (ch < kLatChunks) {
+                        const uint32_t a = tmem + ch * 32;
+                        mma_ts(d, a, bd, idesc, ch != 0);
+                        mma_ts(d, a + 8, bd + 2, idesc, 1u);
+                        mma_ts(d, a + 16, bd + 4, idesc, 1u);
+                        mma_ts(d, a + 24, bd + 6, idesc, 1u);
+                    } else {
+                        mma_ss(d, rope_desc, bd, idesc, 1u);
+                        mma_ss(d, rope_desc + 2, bd + 2, idesc, 1u);
+                        mma_ss(d, rope_desc + 4, bd + 4, idesc, 1u);
+                        mma_ss(d, rope_desc + 6, bd + 6, idesc, 1u);
+                    }
+                }
                 mma_commit(c.bar(B_SFULL + sb));
                 continue;
             }
@@ -1330,7 +1368,7 @@ split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_cons
         if (kFp8 && is_score) {
             if (elect_one_lane()) score_producer_e4m3(p, c, &kv_map, part, warp == 0 ? 0 : 1);
         } else if (kSparse && is_score) {
-            score_producer_sparse(p, c, &kv_map, part, tile, warp == 0 ? 0 : 1);
+            if (warp == 0) score_producer_sparse(p, c, &kv_map, part, tile);
         } else if (kSparse) {
             if (warp == 0) value_producer_sparse(p, c, &kv_map, part, tile);
         } else if (elect_one_lane() && (warp == 0 || (is_score && kScoreIssuers > 1))) {
