@@ -187,7 +187,11 @@ enum Bar {
 // value CTA's read-before-write barrier of the in-place widening
 constexpr int B_VLAND = B_BASE_COUNT, B_SCFULL = B_VLAND + kVStages, B_SCEMPTY = B_SCFULL + kScSlots,
               B_VREAD = B_SCEMPTY + kScSlots;
-constexpr int B_COUNT = kRing ? B_VREAD + 1 : B_BASE_COUNT;
+// sparse lists: one barrier per 64-dim chunk of each page buffer, at the same
+// offset in both CTAs, so that the score MMAs can start on a page's first
+// chunks while the rest are still being gathered
+constexpr int B_CHUNK = B_VREAD + 1;
+constexpr int B_COUNT = kSparse ? B_CHUNK + kVStages * kKChunks : (kRing ? B_VREAD + 1 : B_BASE_COUNT);
 constexpr uint32_t kTmemSlotOff = kBarOff + B_COUNT * 8;
 constexpr uint32_t kAbortOff = kTmemSlotOff + 4;
 constexpr uint32_t kSmemUsed = kAbortOff + 4;
@@ -540,26 +544,26 @@ __device__ void score_producer_sparse(const DecodeParams &p, const Ctx &c, const
                 ok = false;
                 break;
             }
-            if (lane == 0) mbar_arrive_expect_tx(c.bar(B_VFULL + b), kKChunks * kChunkBytes);
+            if (lane < kKChunks) mbar_arrive_expect_tx(c.bar(B_CHUNK + b * kKChunks + lane), kChunkBytes);
             __syncwarp();
             if (lane < 16) {
                 const uint32_t buf = smem_u32(c.base + kKRingOff + b * kVStageBytes) + 512u * (uint32_t)lane;
-                tma_gather4(buf + (uint32_t)kLatChunks * kChunkBytes, map, c.bar(B_VFULL + b), 64 * kLatChunks, y[0],
-                            y[1], y[2], y[3]);
+                tma_gather4(buf + (uint32_t)kLatChunks * kChunkBytes, map, c.bar(B_CHUNK + b * kKChunks + kLatChunks),
+                            64 * kLatChunks, y[0], y[1], y[2], y[3]);
 #pragma unroll
                 for (int ch = 0; ch <= kSparseSplitChunk; ++ch)
                     if (ch < kSparseSplitChunk || lane < 8)
-                        tma_gather4_multicast(buf + (uint32_t)ch * kChunkBytes, map, c.bar(B_VFULL + b), 64 * ch, y[0],
-                                              y[1], y[2], y[3], kPairMask);
+                        tma_gather4_multicast(buf + (uint32_t)ch * kChunkBytes, map, c.bar(B_CHUNK + b * kKChunks + ch),
+                                              64 * ch, y[0], y[1], y[2], y[3], kPairMask);
             }
         }
     }
     // the last pages' bytes (ours and the peer's) must have landed before
     // this CTA may exit (already true on the normal path, where the MMAs
     // waited for them)
-    if (lane == 0)
+    if (lane < kKChunks)
         for (uint32_t k = it > (uint32_t)kVStages ? it - kVStages : 0; k < it; ++k)
-            mbar_wait(c.bar(B_VFULL + (int)(k % kVStages)), (k / kVStages) & 1, c.status);
+            mbar_wait(c.bar(B_CHUNK + (int)(k % kVStages) * kKChunks + lane), (k / kVStages) & 1, c.status);
     __syncwarp();
 }
 
@@ -586,21 +590,21 @@ __device__ void value_producer_sparse(const DecodeParams &p, const Ctx &c, const
                 ok = false;
                 break;
             }
-            if (lane == 0) mbar_arrive_expect_tx(c.bar(B_VFULL + b), kVChunks * kChunkBytes);
+            if (lane < kVChunks) mbar_arrive_expect_tx(c.bar(B_CHUNK + b * kKChunks + lane), kChunkBytes);
             __syncwarp();
             if (lane < 16) {
                 const uint32_t buf = smem_u32(c.base + kVRingOff + b * kVStageBytes) + 512u * (uint32_t)lane;
 #pragma unroll
                 for (int ch = kSparseSplitChunk; ch < kVChunks; ++ch)
                     if (ch > kSparseSplitChunk || lane >= 8)
-                        tma_gather4_multicast(buf + (uint32_t)ch * kChunkBytes, map, c.bar(B_VFULL + b), 64 * ch, y[0],
-                                              y[1], y[2], y[3], kPairMask);
+                        tma_gather4_multicast(buf + (uint32_t)ch * kChunkBytes, map, c.bar(B_CHUNK + b * kKChunks + ch),
+                                              64 * ch, y[0], y[1], y[2], y[3], kPairMask);
             }
         }
     }
-    if (lane == 0)
+    if (lane < kVChunks)
         for (uint32_t k = it > (uint32_t)kVStages ? it - kVStages : 0; k < it; ++k)
-            mbar_wait(c.bar(B_VFULL + (int)(k % kVStages)), (k / kVStages) & 1, c.status);
+            mbar_wait(c.bar(B_CHUNK + (int)(k % kVStages) * kKChunks + lane), (k / kVStages) & 1, c.status);
     __syncwarp();
 }
 
@@ -705,20 +709,24 @@ __device__ void score_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, in
                 continue;
             }
             if constexpr (kSparse) {
-                // one page from page buffer st % 2, all nine chunks at once
+                // one page from page buffer st % 2, each chunk as soon as it
+                // has landed, in the order the two CTAs' gathers complete
                 const int pb = (int)(st % kVStages);
-                if (!wait(c, B_VFULL + pb, (st / kVStages) & 1)) return;
                 const uint32_t buf = ring + pb * kVStageBytes;
-                for (int ch = 0; ch < kKChunks; ++ch) {
+#pragma unroll 1
+                for (int i = 0; i < kKChunks; ++i) {
+                    // 8, then 0, 4, 1, 5, 2, 6, 3, 7: the two CTAs' gather queues interleaved
+                    const int ch = i == 0 ? kLatChunks : (((i - 1) & 1) ? 4 + ((i - 1) >> 1) : ((i - 1) >> 1));
+                    if (!wait(c, B_CHUNK + pb * kKChunks + ch, (st / kVStages) & 1)) return;
                     const uint64_t bd = desc_sw128(buf + ch * kChunkBytes, 16, 1024);
                     if (ch < kLatChunks) {
                         const uint32_t a = tmem + ch * 32;
-                        mma_ts(d, a, bd, idesc, ch != 0);
+                        mma_ts(d, a, bd, idesc, i != 0);
                         mma_ts(d, a + 8, bd + 2, idesc, 1u);
                         mma_ts(d, a + 16, bd + 4, idesc, 1u);
                         mma_ts(d, a + 24, bd + 6, idesc, 1u);
                     } else {
-                        mma_ss(d, rope_desc, bd, idesc, 1u);
+                        mma_ss(d, rope_desc, bd, idesc, i != 0);
                         mma_ss(d, rope_desc + 2, bd + 2, idesc, 1u);
                         mma_ss(d, rope_desc + 4, bd + 4, idesc, 1u);
                         mma_ss(d, rope_desc + 6, bd + 6, idesc, 1u);
@@ -769,7 +777,13 @@ __device__ void value_mma(const DecodeParams &p, const Ctx &c, uint32_t tmem, in
         ++oseg;
         for (int pg = s.p0; pg < s.p1; ++pg, ++it) {
             const int st = it % kVStages, pb = it % kPBufs;
-            if (!wait(c, B_VFULL + st, (it / kVStages) & 1)) return;
+            if constexpr (kSparse) {
+                // every value chunk of the page buffer (gathered by both CTAs)
+                for (int ch = 0; ch < kVChunks; ++ch)
+                    if (!wait(c, B_CHUNK + st * kKChunks + ch, (it / kVStages) & 1)) return;
+            } else if (!wait(c, B_VFULL + st, (it / kVStages) & 1)) {
+                return;
+            }
             if (!wait(c, B_PREADY + pb, (it / kPBufs) & 1)) return;
             tc_fence_after();
             const uint32_t vtile = smem_u32(c.base + kVRingOff + st * kVStageBytes);
@@ -1158,7 +1172,12 @@ __device__ void value_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
             // that garbage (even NaN) times a zero weight stays zero
             const int tail = s.T - pg * kPage;
             if (!kFp8 && tail < kPage) {
-                if (!warp_wait(c, B_VFULL + st, (it / kVStages) & 1)) return;
+                if constexpr (kSparse) {
+                    for (int ch = 0; ch < kVChunks; ++ch)
+                        if (!warp_wait(c, B_CHUNK + st * kKChunks + ch, (it / kVStages) & 1)) return;
+                } else if (!warp_wait(c, B_VFULL + st, (it / kVStages) & 1)) {
+                    return;
+                }
                 uint8_t *vt = c.base + kVRingOff + st * kVStageBytes;
                 const int rows_bad = kPage - tail;
                 for (int idx = tid; idx < kVChunks * rows_bad * 8; idx += 128) {
@@ -1317,6 +1336,7 @@ split_kv_tc_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_cons
                 mbar_init(c.bar(B_SCFULL + i), 1);
                 mbar_init(c.bar(B_SCEMPTY + i), 128);
             }
+            for (int i = 0; i < kVStages * kKChunks; ++i) mbar_init(c.bar(B_CHUNK + i), 1);
         }
         if constexpr (kFp8) {
             for (int i = 0; i < kVStages; ++i) mbar_init(c.bar(B_VLAND + i), 1);
