@@ -328,6 +328,9 @@ def main():
     torch.cuda.set_device(dev)
     import mla_decode_attention_latent_gb300 as mla
     mla._lib.load()
+    if world > 1:
+        # one job across several GPUs: no TMA cluster multicast anywhere
+        mla.mla_set_cluster_multicast(False)
     for name in names:
         line = run_workload(args, mla, W.CASES[name], name, rank, world, local, dev)
         if rank == 0:

@@ -326,6 +326,20 @@ MLA_API int mla_device_status(int *status, int clear);
  */
 MLA_API int mla_set_timing_events(void *split_begin, void *split_end);
 
+/*
+ * mla_set_cluster_multicast — how mla_decode_kvcache_sparse gathers rows.
+ *
+ * With 1 (the default) the two CTAs of a cluster split each list chunk's row
+ * gathers between them and write every gathered row into both CTAs with a
+ * TMA cluster multicast (within this GPU's own memory).  With 0 each CTA
+ * gathers every row chunk it uses itself and nothing is multicast; the
+ * results are bit-identical, the decode about 1.3x slower.  A process that
+ * runs one job across several GPUs sets 0 before its first call.  The
+ * setting is process-wide.  Returns MLA_OK, or MLA_ERR_INVALID_ARG unless
+ * `enabled` is 0 or 1.
+ */
+MLA_API int mla_set_cluster_multicast(int enabled);
+
 /* mla_status_string — static description of a status code (never NULL). */
 MLA_API const char *mla_status_string(int status);
 

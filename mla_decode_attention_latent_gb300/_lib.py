@@ -53,6 +53,7 @@ SIGNATURES = {
                                         _P, _P]),
     "mla_device_status": (_I, [ctypes.POINTER(ctypes.c_int), _I]),
     "mla_set_timing_events": (_I, [_P, _P]),
+    "mla_set_cluster_multicast": (_I, [_I]),
     "mla_status_string": (ctypes.c_char_p, [_I]),
 }
 

@@ -300,6 +300,13 @@ def mla_set_timing_events(split_begin: Optional[torch.cuda.Event], split_end: Op
     check("mla_set_timing_events", load().mla_set_timing_events(b, e))
 
 
+def mla_set_cluster_multicast(enabled: bool) -> None:
+    """Sparse decode: split each list chunk's row gathers between the CTA pair with
+    cluster multicast (True, the default) or have each CTA gather its own rows
+    (False; processes that run one job across several GPUs use this)."""
+    check("mla_set_cluster_multicast", load().mla_set_cluster_multicast(int(bool(enabled))))
+
+
 # the usage page's names for the same two calls
 get_mla_metadata = mla_get_metadata
 flash_mla_with_kvcache = mla_decode_kvcache

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 #include <nvtx3/nvToolsExt.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "mla_internal.h"
@@ -47,6 +48,8 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 constexpr int kRowsPerTile = 128;  // query rows per tensor-core tile
 
 std::mutex g_timing_mutex;
+// sparse decode: pair-split gathers with cluster multicast (1) or local gathers (0)
+std::atomic<int> g_cluster_multicast{1};
 cudaEvent_t g_split_begin = nullptr, g_split_end = nullptr;
 constexpr int kMaxRows = 65536;
 
@@ -185,7 +188,8 @@ int decode(const void *q, const void *kcache, Kind kind, int64_t num_blocks, con
         ev_end = g_split_end;
     }
     if (ev_begin && cudaEventRecord(ev_begin, s) != cudaSuccess) return MLA_ERR_CUDA;
-    cudaError_t e = sparse ? launch_split_kv_tc_sparse(p, s)
+    cudaError_t e = sparse ? (g_cluster_multicast.load() ? launch_split_kv_tc_sparse(p, s)
+                                                         : launch_split_kv_tc_sparse_local(p, s))
                     : e4m3 ? launch_split_kv_tc<576, true>(p, s)
                            : (d == kDqk ? launch_split_kv_tc<576, false>(p, s) : launch_split_kv_tc<512, false>(p, s));
     if (e != cudaSuccess) return MLA_ERR_CUDA;
@@ -253,6 +257,12 @@ int mla_set_timing_events(void *split_begin, void *split_end) {
     std::lock_guard<std::mutex> lock(g_timing_mutex);
     g_split_begin = static_cast<cudaEvent_t>(split_begin);
     g_split_end = static_cast<cudaEvent_t>(split_end);
+    return MLA_OK;
+}
+
+int mla_set_cluster_multicast(int enabled) {
+    if (enabled != 0 && enabled != 1) return MLA_ERR_INVALID_ARG;
+    g_cluster_multicast.store(enabled);
     return MLA_OK;
 }
 

@@ -54,8 +54,11 @@ cudaError_t launch_schedule(const int32_t *seqlens, int batch, int num_parts, in
 // rows or (E4M3, D = 576) packed e4m3 pages with per-token scales
 template <int D, bool E4M3>
 cudaError_t launch_split_kv_tc(const DecodeParams &p, cudaStream_t stream);
-// the sparse top-k variant (576-wide bf16 rows gathered from index lists)
+// the sparse top-k variant (576-wide bf16 rows gathered from index lists):
+// the CTA pair splits each page's gathers with cluster multicast, or (local)
+// each CTA gathers its own rows
 cudaError_t launch_split_kv_tc_sparse(const DecodeParams &p, cudaStream_t stream);
+cudaError_t launch_split_kv_tc_sparse_local(const DecodeParams &p, cudaStream_t stream);
 int split_kv_tc_tile_rows();
 // CTA pairs of the split-KV kernel that fit on the current device at once
 template <int D, bool E4M3>

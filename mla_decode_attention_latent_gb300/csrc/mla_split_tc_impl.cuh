@@ -91,6 +91,12 @@ constexpr bool kFp8 = MLA_SPLIT_FP8 != 0;      // e4m3 cache pages with per-toke
 #define MLA_SPLIT_SPARSE 0
 #endif
 constexpr bool kSparse = MLA_SPLIT_SPARSE != 0;  // keys gathered row by row from per-query-token index lists
+#ifndef MLA_SPARSE_MULTICAST
+#define MLA_SPARSE_MULTICAST 1
+#endif
+// sparse lists: the CTA pair splits each page's row gathers and multicasts
+// them to both CTAs (1), or each CTA gathers every chunk it uses itself (0)
+constexpr bool kPairGather = kSparse && MLA_SPARSE_MULTICAST != 0;
 static_assert(!(kSparse && kFp8) && (!kSparse || MLA_SPLIT_D == 576), "sparse decode: 576-wide bf16 rows");
 constexpr bool kRing = kFp8 || kSparse;          // a per-step side ring (e4m3: token scales; sparse: key masks)
 
@@ -501,7 +507,10 @@ __device__ __forceinline__ uint64_t spread4(uint32_t x) {
 // buffer is refilled only after the value CTA's P V of the page two earlier,
 // which follows the score CTA's MMAs of that page: the value producer waits
 // for it on its own barrier, the score producer on the P-free barrier that
-// the same MMA commit arrives on.
+// the same MMA commit arrives on.  The variant built with
+// MLA_SPARSE_MULTICAST = 0 keeps the buffers, barriers and hand-offs but has
+// each CTA gather every chunk it uses itself, with no multicast: processes
+// that run one job across several GPUs select it (mla_set_cluster_multicast).
 constexpr int kSparseSplitChunk = 3;   // chunks below: the score CTA's; above: the value CTA's; this one by halves
 constexpr uint16_t kPairMask = 0x3;    // both CTAs of the cluster
 
@@ -551,10 +560,17 @@ __device__ void score_producer_sparse(const DecodeParams &p, const Ctx &c, const
                 tma_gather4(buf + (uint32_t)kLatChunks * kChunkBytes, map, c.bar(B_CHUNK + b * kKChunks + kLatChunks),
                             64 * kLatChunks, y[0], y[1], y[2], y[3]);
 #pragma unroll
-                for (int ch = 0; ch <= kSparseSplitChunk; ++ch)
-                    if (ch < kSparseSplitChunk || lane < 8)
-                        tma_gather4_multicast(buf + (uint32_t)ch * kChunkBytes, map, c.bar(B_CHUNK + b * kKChunks + ch),
-                                              64 * ch, y[0], y[1], y[2], y[3], kPairMask);
+                for (int ch = 0; ch < kLatChunks; ++ch) {
+                    if constexpr (kPairGather) {
+                        if (ch < kSparseSplitChunk || (ch == kSparseSplitChunk && lane < 8))
+                            tma_gather4_multicast(buf + (uint32_t)ch * kChunkBytes, map,
+                                                  c.bar(B_CHUNK + b * kKChunks + ch), 64 * ch, y[0], y[1], y[2], y[3],
+                                                  kPairMask);
+                    } else {
+                        tma_gather4(buf + (uint32_t)ch * kChunkBytes, map, c.bar(B_CHUNK + b * kKChunks + ch), 64 * ch,
+                                    y[0], y[1], y[2], y[3]);
+                    }
+                }
             }
         }
     }
@@ -595,10 +611,17 @@ __device__ void value_producer_sparse(const DecodeParams &p, const Ctx &c, const
             if (lane < 16) {
                 const uint32_t buf = smem_u32(c.base + kVRingOff + b * kVStageBytes) + 512u * (uint32_t)lane;
 #pragma unroll
-                for (int ch = kSparseSplitChunk; ch < kVChunks; ++ch)
-                    if (ch > kSparseSplitChunk || lane >= 8)
-                        tma_gather4_multicast(buf + (uint32_t)ch * kChunkBytes, map, c.bar(B_CHUNK + b * kKChunks + ch),
-                                              64 * ch, y[0], y[1], y[2], y[3], kPairMask);
+                for (int ch = 0; ch < kVChunks; ++ch) {
+                    if constexpr (kPairGather) {
+                        if (ch > kSparseSplitChunk || (ch == kSparseSplitChunk && lane >= 8))
+                            tma_gather4_multicast(buf + (uint32_t)ch * kChunkBytes, map,
+                                                  c.bar(B_CHUNK + b * kKChunks + ch), 64 * ch, y[0], y[1], y[2], y[3],
+                                                  kPairMask);
+                    } else {
+                        tma_gather4(buf + (uint32_t)ch * kChunkBytes, map, c.bar(B_CHUNK + b * kKChunks + ch), 64 * ch,
+                                    y[0], y[1], y[2], y[3]);
+                    }
+                }
             }
         }
     }
@@ -1527,8 +1550,10 @@ cudaError_t split_kv_tc_max_pairs<kD, kFp8>(int *pairs) {
 
 #endif
 
-#if MLA_SPLIT_SPARSE
+#if MLA_SPLIT_SPARSE && MLA_SPARSE_MULTICAST
 cudaError_t launch_split_kv_tc_sparse(const DecodeParams &p, cudaStream_t stream) {
+#elif MLA_SPLIT_SPARSE
+cudaError_t launch_split_kv_tc_sparse_local(const DecodeParams &p, cudaStream_t stream) {
 #else
 template <>
 cudaError_t launch_split_kv_tc<kD, kFp8>(const DecodeParams &p, cudaStream_t stream) {

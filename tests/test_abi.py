@@ -266,3 +266,10 @@ def test_header_is_a_c_abi(lib, tmp_path):
                     so, "-Wl,-rpath," + os.path.dirname(so), "-o", exe], check=True)
     out = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert out.returncode == 0 and out.stdout.strip() == "ok", out.stderr
+
+
+def test_cluster_multicast_switch(lib):
+    # a process-wide setting, no device work: only 0 and 1 are accepted
+    assert lib.mla_set_cluster_multicast(2) == _lib.MLA_ERR_INVALID_ARG
+    assert lib.mla_set_cluster_multicast(0) == _lib.MLA_OK
+    assert lib.mla_set_cluster_multicast(1) == _lib.MLA_OK

@@ -425,3 +425,40 @@ def test_sparse_full_list_matches_dense():
     o_d, l_d, *_ = run_gpu(x)
     assert mla.mla_device_status(clear=True) == 0
     assert torch.allclose(o_s.float(), o_d.float(), rtol=1e-2, atol=2e-3) and torch.allclose(l_s, l_d, atol=1e-4)
+
+
+@pytest.fixture
+def no_multicast():
+    import mla_decode_attention_latent_gb300 as mla
+    mla.mla_set_cluster_multicast(False)
+    yield
+    mla.mla_set_cluster_multicast(True)
+
+
+@pytest.mark.parametrize("batch,s_q,h_q,seqlens,topk,parts", [
+    (2, 1, 16, [300, 37], 64, None),
+    (3, 1, 128, [1000, 77, 2100], 256, 3),            # lists cut between parts
+    (2, 2, 128, [700, 130], 100, None),               # two query tokens, a partial last chunk
+])
+def test_sparse_decode_without_multicast(no_multicast, batch, s_q, h_q, seqlens, topk, parts):
+    # each CTA of the pair gathers its own rows (the variant for jobs across several GPUs)
+    sparse_check(batch, s_q, h_q, seqlens, topk, seed=170 + topk + batch, num_parts=parts)
+
+
+def test_sparse_gather_variants_bit_identical():
+    # pair-split multicast gathers and local gathers land the same rows in the
+    # same operand layout, so the full-size outputs must be equal bit for bit
+    import mla_decode_attention_latent_gb300 as mla
+    c = W.CASES["sparse"]
+    x = W.make_inputs(c, device="cuda")
+    o1, l1, _, _, st = run_gpu_sparse(x)
+    assert st == 0, f"device status {st:#x}"
+    mla.mla_set_cluster_multicast(False)
+    try:
+        o2, l2, _, _, st = run_gpu_sparse(x)
+    finally:
+        mla.mla_set_cluster_multicast(True)
+    assert st == 0, f"device status {st:#x}"
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)
+    del x, o1, l1, o2, l2
+    torch.cuda.empty_cache()
