@@ -462,3 +462,15 @@ def test_sparse_gather_variants_bit_identical():
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(l1, l2)
     del x, o1, l1, o2, l2
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("multicast", [True, False])
+def test_sparse_decode_many_small_parts(multicast):
+    # more parts than list chunks: empty parts and parts of one chunk, whose
+    # two producers must still agree on every page buffer's fills
+    import mla_decode_attention_latent_gb300 as mla
+    mla.mla_set_cluster_multicast(multicast)
+    try:
+        sparse_check(3, 1, 128, [900, 40, 2000], 300, seed=181, num_parts=40)
+    finally:
+        mla.mla_set_cluster_multicast(True)
