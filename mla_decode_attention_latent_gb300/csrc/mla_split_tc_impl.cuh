@@ -1201,14 +1201,13 @@ __device__ void value_rows(const DecodeParams &p, const Ctx &c, uint32_t tmem, i
                 } else if (!warp_wait(c, B_VFULL + st, (it / kVStages) & 1)) {
                     return;
                 }
-                uint8_t *vt = c.base + kVRingOff + st * kVStageBytes;
-                const int rows_bad = kPage - tail;
-                for (int idx = tid; idx < kVChunks * rows_bad * 8; idx += 128) {
-                    const int ch = idx / (rows_bad * 8);
-                    const int rr = tail + (idx / 8) % rows_bad;
-                    const int piece = idx % 8;
-                    *reinterpret_cast<uint4 *>(vt + ch * kChunkBytes + rr * 128 + piece * 16) = make_uint4(0, 0, 0, 0);
-                }
+                // thread t zeroes 16-byte piece t % 8 of rows tail + t / 8,
+                // + 16, ... in every chunk (whole 128-byte rows, so the swizzle
+                // does not matter)
+                const uint32_t vt = smem_u32(c.base + kVRingOff + st * kVStageBytes) + 16u * (uint32_t)(tid & 7);
+                for (int rr = (tail > 0 ? tail : 0) + (tid >> 3); rr < kPage; rr += 16)
+#pragma unroll
+                    for (int ch = 0; ch < kVChunks; ++ch) sts128(vt + ch * kChunkBytes + rr * 128, 0u, 0u, 0u, 0u);
                 fence_proxy_async_smem();
             }
             // lazy rescale of this row of O before the next accumulation
