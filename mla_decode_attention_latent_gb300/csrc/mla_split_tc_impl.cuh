@@ -29,8 +29,9 @@
 //   TMA: 16 KB chunk slots, each holding       into a 2-stage ring
 //     one 64-dim chunk of two pages          tcgen05 O += P V  (N = 2 x 256)
 //   tcgen05 S = Q K^T over two pages at      4 warps: zero the tail rows of V,
-//     once (N = 128: full tensor rate),        lazy O rescale, epilogue staged
-//     two issuers alternating steps            through smem
+//     once (N = 128), A from TMEM (the         lazy O rescale, epilogue staged
+//     RoPE chunk's from smem), two issuers     through smem
+//     alternating steps
 //   4 warps: mask + online softmax; P and
 //     row factors -> local staging -> bulk
 //     copies into the value CTA
