@@ -348,6 +348,14 @@ HOLD_S_PER_STEP = 300e-6     # host time to enqueue one timed step (flush, event
 ALL_WORKLOADS = ["tiny", "uniform", "variable", "mtp", "long", "uniform_d512", "uniform_fp8", "sparse"]
 
 
+def partition(mla, case, lens, num_parts=None):
+    """The work partition as a caller of this workload computes it: a sparse
+    workload over its list lengths with the sparse decode's costs."""
+    if case.topk:
+        return mla.mla_get_metadata_sparse(lens, case.num_q_rows, case.h_kv, num_parts=num_parts)
+    return mla.mla_get_metadata(lens, case.num_q_rows, case.h_kv, num_parts=num_parts)
+
+
 def run_workload(args, mla, case, name, rank, world, local, dev):
     """Time one workload; returns rank 0's JSON line (None on other ranks)."""
     from mla_decode_attention_latent_gb300 import workloads as W
@@ -361,7 +369,7 @@ def run_workload(args, mla, case, name, rank, world, local, dev):
     # the work partition runs on the cache lengths, or on the list lengths (sparse)
     part_lens = (torch.full((case.batch,), case.topk, dtype=torch.int32, device=dev) if case.topk
                  else x.cache_seqlens)
-    md, ns = mla.mla_get_metadata(part_lens, case.num_q_rows, case.h_kv)
+    md, ns = partition(mla, case, part_lens)
     num_parts = md.shape[0]
     o = torch.empty((case.batch, case.s_q, case.h_q, case.dv), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((case.batch, case.s_q, case.h_q), dtype=torch.float32, device=dev)
@@ -372,7 +380,7 @@ def run_workload(args, mla, case, name, rank, world, local, dev):
 
     def step(md_k=None, ns_k=None):
         if md_k is None:
-            md_k, ns_k = mla.mla_get_metadata(part_lens, case.num_q_rows, case.h_kv, num_parts=num_parts)
+            md_k, ns_k = partition(mla, case, part_lens, num_parts)
         if case.topk:
             mla.mla_decode_kvcache_sparse(x.q, x.kcache, x.block_table, x.cache_seqlens, x.indices, case.dv, md_k,
                                           ns_k, list_lens=part_lens, softmax_scale=case.softmax_scale, out=o, lse=lse,
@@ -451,7 +459,7 @@ def run_workload(args, mla, case, name, rank, world, local, dev):
     mla.mla_set_timing_events(None, None)
     # timed region 3 (decode_only): the decode call alone, with the metadata
     # of the first step reused by every later one (as every layer reuses it)
-    md_once, ns_once = mla.mla_get_metadata(part_lens, case.num_q_rows, case.h_kv, num_parts=num_parts)
+    md_once, ns_once = partition(mla, case, part_lens, num_parts)
     barrier(world)
     torch.cuda.synchronize()
     torch.cuda.nvtx.range_push("decode_only")
@@ -558,7 +566,7 @@ def e2e_run(mla, case, x, fig, dev, stream, steps, world):
             d["copied"].record(copy_stream)
         stream.wait_event(d["copied"])
         if case.topk:
-            md, ns = mla.mla_get_metadata(lens, case.num_q_rows, case.h_kv)
+            md, ns = partition(mla, case, lens)
             o, lse = mla.mla_decode_kvcache_sparse(d["q"], d["k"], d["bt"], d["sl"], d["idx"], case.dv, md, ns,
                                                    list_lens=lens, softmax_scale=case.softmax_scale)
         else:

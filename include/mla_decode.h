@@ -84,6 +84,14 @@ struct CUstream_st;
 #define MLA_SCHED_FIXED_COST_PAGES 8
 /* cost, in pages, that the partition charges for needing the combine pass */
 #define MLA_SCHED_COMBINE_COST_PAGES 4
+/* the same two costs for the sparse decode, in 64-entry list chunks: a list
+   chunk's row gathers take about four times a dense page, so the per-segment
+   costs come to about a quarter (measured on GB300: topk 2048 over b = 64
+   sequences, split kernel 167 us with the dense costs, 152 us with these) */
+#define MLA_SCHED_SPARSE_FIXED_COST_CHUNKS 2
+#define MLA_SCHED_SPARSE_COMBINE_COST_CHUNKS 1
+/* largest cost mla_get_metadata_costs accepts */
+#define MLA_SCHED_MAX_COST (1 << 20)
 
 /* device-side error bits reported through mla_device_status() */
 #define MLA_DEVERR_TIMEOUT 0x1     /* a bounded wait inside a kernel gave up */
@@ -136,6 +144,23 @@ MLA_API int mla_num_sm_parts(int device, int num_q_rows, int h_kv, int *num_part
 MLA_API int mla_get_metadata(const int32_t *cache_seqlens, int batch, int num_q_rows, int h_kv,
                      int num_parts, int32_t *tile_scheduler_metadata, int32_t *num_splits,
                      struct CUstream_st *stream);
+
+/*
+ * mla_get_metadata_costs — the same partition with the two costs given.
+ *
+ * mla_get_metadata is this call with fixed_cost = MLA_SCHED_FIXED_COST_PAGES
+ * and combine_cost = MLA_SCHED_COMBINE_COST_PAGES.  The costs are in units
+ * of one page of the lengths the partition is computed on (for the sparse
+ * decode: one 64-entry list chunk; MLA_SCHED_SPARSE_*_CHUNKS are its
+ * measured values).  They change only how the work is cut, never what a
+ * decode computes.
+ *   fixed_cost    cost of one segment (>= 1, <= MLA_SCHED_MAX_COST)
+ *   combine_cost  cost charged for needing the combine (>= 0, <= MLA_SCHED_MAX_COST)
+ * Other arguments, outputs and errors: as mla_get_metadata.
+ */
+MLA_API int mla_get_metadata_costs(const int32_t *cache_seqlens, int batch, int num_q_rows, int h_kv,
+                           int num_parts, int fixed_cost, int combine_cost, int32_t *tile_scheduler_metadata,
+                           int32_t *num_splits, struct CUstream_st *stream);
 
 /*
  * mla_workspace_bytes — device scratch that mla_decode_kvcache needs for the

@@ -42,6 +42,7 @@ _P, _I, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_
 SIGNATURES = {
     "mla_num_sm_parts": (_I, [_I, _I, _I, ctypes.POINTER(ctypes.c_int)]),
     "mla_get_metadata": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
+    "mla_get_metadata_costs": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "mla_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "mla_decode_kvcache": (_I, [_P, _P, _I64, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _F, _I, _P, _P,
                                 _P, _SZ, _P]),

@@ -47,9 +47,21 @@ def mla_num_sm_parts(num_q_rows: int, h_kv: int = 1, device: Optional[torch.devi
     return out.value
 
 
+# the partition's costs (include/mla_decode.h): per segment and for needing
+# the combine, in pages of the lengths the partition is computed on
+SCHED_FIXED_COST_PAGES = 8
+SCHED_COMBINE_COST_PAGES = 4
+SCHED_SPARSE_FIXED_COST_CHUNKS = 2
+SCHED_SPARSE_COMBINE_COST_CHUNKS = 1
+
+
 def mla_get_metadata(cache_seqlens: torch.Tensor, num_q_rows: int, h_kv: int = 1,
-                     num_parts: Optional[int] = None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Split-KV work partition: (tile_scheduler_metadata int32 [P, 8], num_splits int32 [b + 1])."""
+                     num_parts: Optional[int] = None, fixed_cost: Optional[int] = None,
+                     combine_cost: Optional[int] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Split-KV work partition: (tile_scheduler_metadata int32 [P, 8], num_splits int32 [b + 1]).
+
+    ``fixed_cost`` / ``combine_cost`` override the partition's costs
+    (``mla_get_metadata_costs``); by default those of a dense decode."""
     _need_cuda("cache_seqlens", cache_seqlens, torch.int32)
     dev = cache_seqlens.device
     if num_parts is None:
@@ -58,10 +70,26 @@ def mla_get_metadata(cache_seqlens: torch.Tensor, num_q_rows: int, h_kv: int = 1
     md = torch.empty((num_parts, MLA_METADATA_INTS), dtype=torch.int32, device=dev)
     ns = torch.empty((batch + 1,), dtype=torch.int32, device=dev)
     with torch.cuda.device(dev):
-        st = load().mla_get_metadata(cache_seqlens.data_ptr(), batch, int(num_q_rows), int(h_kv), int(num_parts),
-                                     md.data_ptr(), ns.data_ptr(), _stream_handle(dev))
+        if fixed_cost is None and combine_cost is None:
+            st = load().mla_get_metadata(cache_seqlens.data_ptr(), batch, int(num_q_rows), int(h_kv), int(num_parts),
+                                         md.data_ptr(), ns.data_ptr(), _stream_handle(dev))
+        else:
+            fc = SCHED_FIXED_COST_PAGES if fixed_cost is None else int(fixed_cost)
+            cc = SCHED_COMBINE_COST_PAGES if combine_cost is None else int(combine_cost)
+            st = load().mla_get_metadata_costs(cache_seqlens.data_ptr(), batch, int(num_q_rows), int(h_kv),
+                                               int(num_parts), fc, cc, md.data_ptr(), ns.data_ptr(),
+                                               _stream_handle(dev))
     check("mla_get_metadata", st)
     return md, ns
+
+
+def mla_get_metadata_sparse(list_lens: torch.Tensor, num_q_rows: int, h_kv: int = 1,
+                            num_parts: Optional[int] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """The work partition of a sparse decode: over the index lists' lengths,
+    with the sparse decode's costs (a 64-entry list chunk's gathers take about
+    four dense pages' time, so the per-segment costs are about a quarter)."""
+    return mla_get_metadata(list_lens, num_q_rows, h_kv, num_parts, fixed_cost=SCHED_SPARSE_FIXED_COST_CHUNKS,
+                            combine_cost=SCHED_SPARSE_COMBINE_COST_CHUNKS)
 
 
 def mla_workspace_bytes(batch: int, s_q: int, h_q: int, h_kv: int, dv: int, num_parts: int) -> int:

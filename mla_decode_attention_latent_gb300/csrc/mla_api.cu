@@ -91,17 +91,26 @@ int mla_num_sm_parts(int device, int num_q_rows, int h_kv, int *num_parts) {
     return MLA_OK;
 }
 
-int mla_get_metadata(const int32_t *cache_seqlens, int batch, int num_q_rows, int h_kv, int num_parts,
-                     int32_t *tile_scheduler_metadata, int32_t *num_splits, struct CUstream_st *stream) {
+int mla_get_metadata_costs(const int32_t *cache_seqlens, int batch, int num_q_rows, int h_kv, int num_parts,
+                           int fixed_cost, int combine_cost, int32_t *tile_scheduler_metadata, int32_t *num_splits,
+                           struct CUstream_st *stream) {
     if (!cache_seqlens || !tile_scheduler_metadata || !num_splits) return MLA_ERR_INVALID_ARG;
     if (batch < 1 || num_q_rows < 1 || h_kv < 1 || num_parts < 1) return MLA_ERR_INVALID_ARG;
+    if (fixed_cost < 1 || fixed_cost > MLA_SCHED_MAX_COST || combine_cost < 0 || combine_cost > MLA_SCHED_MAX_COST)
+        return MLA_ERR_INVALID_ARG;
     if (h_kv != 1) return MLA_ERR_UNSUPPORTED;
     Range range("mla_get_metadata");
     unsigned int *status = nullptr;
     if (status_address(&status) != MLA_OK) return MLA_ERR_CUDA;
-    cudaError_t e = launch_schedule(cache_seqlens, batch, num_parts, tile_scheduler_metadata, num_splits, status,
-                                    reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_schedule(cache_seqlens, batch, num_parts, fixed_cost, combine_cost, tile_scheduler_metadata,
+                                    num_splits, status, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+int mla_get_metadata(const int32_t *cache_seqlens, int batch, int num_q_rows, int h_kv, int num_parts,
+                     int32_t *tile_scheduler_metadata, int32_t *num_splits, struct CUstream_st *stream) {
+    return mla_get_metadata_costs(cache_seqlens, batch, num_q_rows, h_kv, num_parts, kFixedCost, kCombineCost,
+                                  tile_scheduler_metadata, num_splits, stream);
 }
 
 size_t mla_workspace_bytes(int batch, int s_q, int h_q, int h_kv, int dv, int num_parts) {

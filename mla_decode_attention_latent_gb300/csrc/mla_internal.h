@@ -48,8 +48,8 @@ struct DecodeParams {
 size_t workspace_bytes(int batch, int rows, int num_parts);
 void carve_workspace(void *ws, int batch, int rows, int num_parts, float **o_accum, float **lse_accum);
 
-cudaError_t launch_schedule(const int32_t *seqlens, int batch, int num_parts, int32_t *metadata,
-                            int32_t *num_splits, unsigned int *status, cudaStream_t stream);
+cudaError_t launch_schedule(const int32_t *seqlens, int batch, int num_parts, int fixed_cost, int combine_cost,
+                            int32_t *metadata, int32_t *num_splits, unsigned int *status, cudaStream_t stream);
 // the tensor-core split-KV kernel for cached rows of width D (576 or 512), bf16
 // rows or (E4M3, D = 576) packed e4m3 pages with per-token scales
 template <int D, bool E4M3>

@@ -6,7 +6,7 @@
 // from cache_seqlens once per decode step; every layer then reuses them.  The
 // page names the outputs only; the partition below is this library's:
 //   lay the sequences on one line of cost units, sequence b taking
-//   c_b = F + n_b units (F = fixed cost of a segment, n_b = ceil(T_b / 64)
+//   c_b = F + n_b units (F = fixed cost of a segment, a call argument; n_b = ceil(T_b / 64)
 //   pages) from S_b = c_0 + ... + c_{b-1}; Q = ceil(total / parts); part p
 //   starts at unit p * Q.  A unit in a sequence's first F units maps to its
 //   page 0, a later one to page (x - S_b - F); the last part ends at
@@ -59,7 +59,7 @@ __device__ T block_exclusive_scan(T v, T *s_warp, T *total) {
 // first unit, so a unit is located by a binary search over the chunks and a
 // short walk inside one.
 __global__ void __launch_bounds__(kSchedThreads)
-schedule_kernel(const int32_t *__restrict__ seqlens, int batch, int num_parts,
+schedule_kernel(const int32_t *__restrict__ seqlens, int batch, int num_parts, int fixed_cost, int combine_cost,
                 int32_t *__restrict__ metadata, int32_t *__restrict__ num_splits,
                 unsigned int *status) {
     __shared__ long long s_start[kSchedThreads + 1];  // first unit of every chunk; [kSchedThreads] = total
@@ -76,7 +76,7 @@ schedule_kernel(const int32_t *__restrict__ seqlens, int batch, int num_parts,
     for (int i = i0; i < i1; ++i) {
         const int t = seqlens[i];
         bad |= t < 0;
-        cost += pages_of(t) + kFixedCost;
+        cost += pages_of(t) + fixed_cost;
     }
     if (bad) atomicOr(status, MLA_DEVERR_SEQLEN);
     long long total;
@@ -95,18 +95,18 @@ schedule_kernel(const int32_t *__restrict__ seqlens, int batch, int num_parts,
         long long u = first_unit;
         for (int i = i0; i < i1; ++i) {
             const int n = pages_of(seqlens[i]);
-            const long long next = u + n + kFixedCost;
+            const long long next = u + n + fixed_cost;
             if (n > 0) {
-                cut_all |= (next - 1) / q_all > (u + kFixedCost) / q_all;
-                cut_seq |= (next - 1) / q_seq > (u + kFixedCost) / q_seq;
+                cut_all |= (next - 1) / q_all > (u + fixed_cost) / q_all;
+                cut_seq |= (next - 1) / q_seq > (u + fixed_cost) / q_seq;
             }
             u = next;
         }
     }
     cut_all = __syncthreads_or(cut_all);
     cut_seq = __syncthreads_or(cut_seq);
-    const long long est_all = q_all + (cut_all ? kFixedCost + kCombineCost : 0);
-    const long long est_seq = q_seq + (cut_seq ? kFixedCost + kCombineCost : 0);
+    const long long est_all = q_all + (cut_all ? fixed_cost + combine_cost : 0);
+    const long long est_seq = q_seq + (cut_seq ? fixed_cost + combine_cost : 0);
     const long long quota = (batch < num_parts && est_seq < est_all) ? q_seq : q_all;
 
     // cursor of unit x: sequence b, page, and S_b
@@ -126,7 +126,7 @@ schedule_kernel(const int32_t *__restrict__ seqlens, int batch, int num_parts,
         long long u = s_start[lo];
         int i = lo * chunk;
         while (true) {
-            const long long c = pages_of(seqlens[i]) + kFixedCost;
+            const long long c = pages_of(seqlens[i]) + fixed_cost;
             if (x < u + c) break;
             u += c;
             ++i;
@@ -134,7 +134,7 @@ schedule_kernel(const int32_t *__restrict__ seqlens, int batch, int num_parts,
         b = i;
         sb = u;
         const long long off = x - u;
-        pg = off <= kFixedCost ? 0 : (int)(off - kFixedCost);
+        pg = off <= fixed_cost ? 0 : (int)(off - fixed_cost);
     };
 
     for (int p = threadIdx.x; p < num_parts; p += kSchedThreads) {
@@ -144,7 +144,7 @@ schedule_kernel(const int32_t *__restrict__ seqlens, int batch, int num_parts,
         if (p + 1 < num_parts) cursor((long long)(p + 1) * quota, b1, pg1, s1);
         // parts touching b0 before p: the one holding its page 0, then every
         // part that started inside its pages (the first at floor((S + F) / Q) + 1)
-        const int split0 = pg0 > 0 ? (int)(p - (s0 + kFixedCost) / quota) : 0;
+        const int split0 = pg0 > 0 ? (int)(p - (s0 + fixed_cost) / quota) : 0;
         int32_t *row = metadata + (size_t)p * kMdInts;  // 4-byte alignment is all the caller promises
         row[0] = b0;
         row[1] = pg0;
@@ -162,8 +162,8 @@ schedule_kernel(const int32_t *__restrict__ seqlens, int batch, int num_parts,
         long long u = first_unit;
         for (int i = i0; i < i1; ++i) {
             const int n = pages_of(seqlens[i]);
-            const long long next = u + n + kFixedCost;
-            segs += 1 + (n > 0 ? (int)((next - 1) / quota - (u + kFixedCost) / quota) : 0);
+            const long long next = u + n + fixed_cost;
+            segs += 1 + (n > 0 ? (int)((next - 1) / quota - (u + fixed_cost) / quota) : 0);
             u = next;
         }
     }
@@ -173,8 +173,8 @@ schedule_kernel(const int32_t *__restrict__ seqlens, int batch, int num_parts,
         long long u = first_unit;
         for (int i = i0; i < i1; ++i) {
             const int n = pages_of(seqlens[i]);
-            const long long next = u + n + kFixedCost;
-            run += 1 + (n > 0 ? (int)((next - 1) / quota - (u + kFixedCost) / quota) : 0);
+            const long long next = u + n + fixed_cost;
+            run += 1 + (n > 0 ? (int)((next - 1) / quota - (u + fixed_cost) / quota) : 0);
             num_splits[i + 1] = run;
             u = next;
         }
@@ -184,10 +184,10 @@ schedule_kernel(const int32_t *__restrict__ seqlens, int batch, int num_parts,
 
 }  // namespace
 
-cudaError_t launch_schedule(const int32_t *seqlens, int batch, int num_parts, int32_t *metadata,
-                            int32_t *num_splits, unsigned int *status, cudaStream_t stream) {
-    schedule_kernel<<<1, kSchedThreads, 0, stream>>>(seqlens, batch, num_parts, metadata, num_splits,
-                                                     status);
+cudaError_t launch_schedule(const int32_t *seqlens, int batch, int num_parts, int fixed_cost, int combine_cost,
+                            int32_t *metadata, int32_t *num_splits, unsigned int *status, cudaStream_t stream) {
+    schedule_kernel<<<1, kSchedThreads, 0, stream>>>(seqlens, batch, num_parts, fixed_cost, combine_cost, metadata,
+                                                     num_splits, status);
     return cudaGetLastError();
 }
 

@@ -51,6 +51,22 @@ def test_fixed_cost_matches_oracle_partition():
     assert int(m.group(1)) == oracle.SCHED_COMBINE_COST_PAGES
 
 
+def test_partition_costs_match_binding():
+    from mla_decode_attention_latent_gb300 import api
+    text = open(HEADER).read()
+    for name in ("SCHED_FIXED_COST_PAGES", "SCHED_COMBINE_COST_PAGES", "SCHED_SPARSE_FIXED_COST_CHUNKS",
+                 "SCHED_SPARSE_COMBINE_COST_CHUNKS"):
+        m = re.search(rf"#define MLA_{name} (\d+)", text)
+        assert m and int(m.group(1)) == getattr(api, name), name
+
+
+@pytest.mark.parametrize("fixed,combine", [(0, 4), (-1, 4), (8, -1), ((1 << 20) + 1, 4), (8, (1 << 20) + 1)])
+def test_metadata_costs_rejected_before_launch(lib, fixed, combine):
+    # out-of-range costs are refused before any pointer is used
+    st = lib.mla_get_metadata_costs(16, 4, 128, 1, 76, fixed, combine, 16, 16, None)
+    assert st == _lib.MLA_ERR_INVALID_ARG
+
+
 def test_status_strings(lib):
     for code in (0, -1, -2, -3, -4, -5, 7):
         assert isinstance(lib.mla_status_string(code), bytes)

@@ -121,6 +121,26 @@ def test_scheduler_matches_oracle_partition():
         assert np.array_equal(ns.cpu().numpy(), ns_ref), trial
 
 
+@pytest.mark.parametrize("fixed,combine", [(1, 0), (2, 1), (8, 4), (40, 100)])
+def test_scheduler_costs_match_oracle_partition(fixed, combine):
+    # the partition with the segment and combine costs given by the caller
+    # (the sparse decode's, the dense default, and extremes that make the
+    # one-part-per-sequence choice go both ways) equals the oracle's
+    import mla_decode_attention_latent_gb300 as mla
+    rng = np.random.default_rng(fixed * 1000 + combine)
+    for trial in range(10):
+        batch = int(rng.integers(1, 200))
+        sl = rng.integers(0, 9000, size=batch).astype(np.int32)
+        if trial % 3 == 0:
+            sl[:] = sl[0]  # equal lengths: the case the part-count choice decides
+        parts = int(rng.integers(1, 160))
+        md, ns = mla.mla_get_metadata(torch.from_numpy(sl).to(DEV), 128, 1, num_parts=parts, fixed_cost=fixed,
+                                      combine_cost=combine)
+        md_ref, ns_ref = oracle.schedule(sl, parts, fixed_cost=fixed, combine_cost=combine)
+        assert np.array_equal(md.cpu().numpy(), md_ref), trial
+        assert np.array_equal(ns.cpu().numpy(), ns_ref), trial
+
+
 @pytest.mark.parametrize("batch,parts", [(9000, 152), (300, 600), (8191, 256), (8192, 257), (1, 1), (5, 1000)])
 def test_scheduler_large_batches_and_part_counts(batch, parts):
     # batches larger than the scheduler's 512 threads (each thread then owns a
@@ -234,7 +254,7 @@ def run_gpu_sparse(x):
     import mla_decode_attention_latent_gb300 as mla
     c = x.case
     lens = torch.full((c.batch,), c.topk, dtype=torch.int32, device=x.q.device)
-    md, ns = mla.mla_get_metadata(lens, c.num_q_rows, c.h_kv)
+    md, ns = mla.mla_get_metadata_sparse(lens, c.num_q_rows, c.h_kv)
     o, lse = mla.mla_decode_kvcache_sparse(x.q, x.kcache, x.block_table, x.cache_seqlens, x.indices, c.dv, md, ns,
                                            list_lens=lens, softmax_scale=c.softmax_scale)
     torch.cuda.synchronize()
@@ -367,7 +387,7 @@ def test_large_q_len(batch, s_q, h_q, seqlens):
 
 
 # ---------------------------------------------------------------- sparse top-k decode
-def sparse_check(batch, s_q, h_q, seqlens, topk, seed, num_parts=None, edit_lists=None):
+def sparse_check(batch, s_q, h_q, seqlens, topk, seed, num_parts=None, edit_lists=None, sparse_costs=False):
     import mla_decode_attention_latent_gb300 as mla
     c = case("sparse", batch, s_q, h_q, seqlens, seed=seed)
     x = W.make_inputs(c, "cpu")
@@ -378,7 +398,8 @@ def sparse_check(batch, s_q, h_q, seqlens, topk, seed, num_parts=None, edit_list
                                               x.cache_seqlens.numpy(), idx.numpy(), c.dv, c.softmax_scale)
     xd = to_device(x, DEV)
     lens = torch.full((batch,), topk, dtype=torch.int32, device=DEV)
-    md, ns = mla.mla_get_metadata(lens, c.num_q_rows, 1, num_parts=num_parts)
+    get_md = mla.mla_get_metadata_sparse if sparse_costs else mla.mla_get_metadata
+    md, ns = get_md(lens, c.num_q_rows, 1, num_parts=num_parts)
     o, lse = mla.mla_decode_kvcache_sparse(xd.q, xd.kcache, xd.block_table, xd.cache_seqlens, idx.to(DEV), c.dv,
                                            md, ns, list_lens=lens, softmax_scale=c.softmax_scale)
     torch.cuda.synchronize()
@@ -398,6 +419,18 @@ def sparse_check(batch, s_q, h_q, seqlens, topk, seed, num_parts=None, edit_list
 ])
 def test_sparse_decode(batch, s_q, h_q, seqlens, topk, parts):
     sparse_check(batch, s_q, h_q, seqlens, topk, seed=150 + topk + batch, num_parts=parts)
+
+
+@pytest.mark.parametrize("batch,topk,parts", [(8, 512, 12), (5, 2048, 76), (3, 300, None)])
+def test_sparse_decode_with_sparse_costs(batch, topk, parts):
+    # the partition with the sparse decode's costs cuts equal-length lists
+    # across more parts than sequences (split sequences, so the combine runs)
+    import mla_decode_attention_latent_gb300 as mla
+    lens = torch.full((batch,), topk, dtype=torch.int32, device=DEV)
+    _, ns = mla.mla_get_metadata_sparse(lens, 128, 1, num_parts=parts)
+    if parts is not None and parts > batch:
+        assert int(ns[-1]) > batch  # some sequence is split
+    sparse_check(batch, 1, 128, [4096] * batch, topk, seed=190 + batch, num_parts=parts, sparse_costs=True)
 
 
 def test_sparse_decode_junk_entries():
