@@ -280,8 +280,10 @@ MLA_API int mla_decode_kvcache_fp8(const void *q, const void *kv_pages, int64_t 
  *   topk           entries per list, >= 1
  *   list_lens      device int32 [batch]: the lengths the work partition was
  *                  computed on (tile_scheduler_metadata and num_splits come
- *                  from mla_get_metadata on this array; normally topk for
- *                  every sequence)
+ *                  from mla_get_metadata_costs on this array with
+ *                  MLA_SCHED_SPARSE_FIXED_COST_CHUNKS and
+ *                  MLA_SCHED_SPARSE_COMBINE_COST_CHUNKS, or from
+ *                  mla_get_metadata; normally topk for every sequence)
  * A 128-row tile holds one query token's heads: s_q must be 1, or h_q 128
  * (MLA_ERR_UNSUPPORTED otherwise).  Rows are gathered one by one from the
  * cache (TMA gathers over the cache viewed as num_blocks * 64 rows, which

@@ -234,7 +234,8 @@ def mla_decode_kvcache_sparse(q: torch.Tensor, kcache: torch.Tensor, block_table
     """Sparse top-k MLA decode: query token i of sequence b attends to the cache
     positions ``indices[b, i]`` (int32 [b, s_q, topk]; entries outside
     [0, cache_seqlens[b]) are ignored).  The work partition is computed on
-    ``list_lens`` (default: topk for every sequence) unless given.  Returns
+    ``list_lens`` (default: topk for every sequence) with the sparse decode's
+    costs (``mla_get_metadata_sparse``) unless given.  Returns
     (o bf16 [b, s_q, h_q, dv], lse fp32 [b, s_q, h_q]); see ``include/mla_decode.h``."""
     for name, t, dt in (("q", q, torch.bfloat16), ("kcache", kcache, torch.bfloat16),
                         ("block_table", block_table, torch.int32), ("cache_seqlens", cache_seqlens, torch.int32),
@@ -252,7 +253,7 @@ def mla_decode_kvcache_sparse(q: torch.Tensor, kcache: torch.Tensor, block_table
         list_lens = torch.full((b,), topk, dtype=torch.int32, device=dev)
     _need_cuda("list_lens", list_lens, torch.int32)
     if tile_scheduler_metadata is None or num_splits is None:
-        tile_scheduler_metadata, num_splits = mla_get_metadata(list_lens, s_q * h_q // h_kv, h_kv)
+        tile_scheduler_metadata, num_splits = mla_get_metadata_sparse(list_lens, s_q * h_q // h_kv, h_kv)
     _need_cuda("tile_scheduler_metadata", tile_scheduler_metadata, torch.int32)
     _need_cuda("num_splits", num_splits, torch.int32)
     if (block_table.dim() != 2 or block_table.shape[0] != b or cache_seqlens.numel() != b or list_lens.numel() != b
