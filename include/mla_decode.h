@@ -86,9 +86,10 @@ struct CUstream_st;
 #define MLA_SCHED_COMBINE_COST_PAGES 4
 /* the same two costs for the sparse decode, in 64-entry list chunks: a list
    chunk's row gathers take about four times a dense page, so the per-segment
-   costs come to about a quarter (measured on GB300: topk 2048 over b = 64
-   sequences, split kernel 167 us with the dense costs, 152 us with these) */
-#define MLA_SCHED_SPARSE_FIXED_COST_CHUNKS 2
+   costs come to a quarter or less (measured on GB300: topk 2048 over b = 64
+   sequences, split + combine 170 us with the dense costs, 156 us with a
+   fixed cost of 2 chunks, 153 us with 1) */
+#define MLA_SCHED_SPARSE_FIXED_COST_CHUNKS 1
 #define MLA_SCHED_SPARSE_COMBINE_COST_CHUNKS 1
 /* largest cost mla_get_metadata_costs accepts */
 #define MLA_SCHED_MAX_COST (1 << 20)

@@ -51,7 +51,7 @@ def mla_num_sm_parts(num_q_rows: int, h_kv: int = 1, device: Optional[torch.devi
 # the combine, in pages of the lengths the partition is computed on
 SCHED_FIXED_COST_PAGES = 8
 SCHED_COMBINE_COST_PAGES = 4
-SCHED_SPARSE_FIXED_COST_CHUNKS = 2
+SCHED_SPARSE_FIXED_COST_CHUNKS = 1
 SCHED_SPARSE_COMBINE_COST_CHUNKS = 1
 
 
