@@ -121,7 +121,7 @@ def test_scheduler_matches_oracle_partition():
         assert np.array_equal(ns.cpu().numpy(), ns_ref), trial
 
 
-@pytest.mark.parametrize("fixed,combine", [(1, 0), (2, 1), (8, 4), (40, 100)])
+@pytest.mark.parametrize("fixed,combine", [(1, 0), (1, 1), (2, 1), (8, 4), (40, 100)])
 def test_scheduler_costs_match_oracle_partition(fixed, combine):
     # the partition with the segment and combine costs given by the caller
     # (the sparse decode's, the dense default, and extremes that make the
